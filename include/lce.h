@@ -1,0 +1,141 @@
+/*
+ * lce.h -- memory-bounded fused linear cross-entropy on GB300 (sm_103a): the C ABI.
+ *
+ * What is computed
+ *   For hidden states H [N x d], a vocabulary projection W [V x d] and labels y [N]:
+ *     logits  Z = H W^T                                      (never stored)
+ *     lse_i   = log sum_v exp(Z_iv)
+ *     loss    = sum over valid rows of (lse_i - Z_{i,y_i}), divided by n_valid for MEAN
+ *     dH      = G W,  dW = G^T H,  G = scale * (softmax(Z) - onehot(y)) on valid rows, 0 elsewhere
+ *   "Long-Sequence MoE RL" blog, section "Linear CE: Avoiding Materialization of Full Logits":
+ *   the linear output and the cross-entropy are organised so that the full logits are never
+ *   generated or retained.  "Flattening Every Memory Peak in Long-Context MoE Training",
+ *   section 3.2 and appendix C (Ring-DTP): each logit strip of the vocabulary is folded into a
+ *   running per-token state and released, and backward recomputes each strip's gradient, so
+ *   neither the full logits nor the full logit gradient is stored; section 2: the values and
+ *   gradients equal those of the dense implementation, only the order of computation changes.
+ *   On one GPU the strips are visited by a local loop; the per-token state is the online
+ *   log-sum-exp triple (running max, running sum of exp, target logit).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers to dense row-major arrays on the current device.
+ *     H and W hold bf16 (LCE_BF16) or fp32 (LCE_F32) values; dH and dW are always fp32.
+ *     labels are int64.  Every pointer must be 16-byte aligned.
+ *   - stream is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every call
+ *     only enqueues work on that stream and returns; nothing is synchronised except in
+ *     lce_check_error.
+ *   - Ownership: the caller owns every buffer, including the workspace.  The library never
+ *     allocates or frees device memory and keeps no pointer after a call returns.
+ *   - Errors: argument and shape problems are found on the host before anything is enqueued
+ *     and returned as a status; nothing is launched then.  Problems found on the device (a
+ *     label outside [0, V) that is not ignore_index; a kernel wait that ran out of time) set a
+ *     flag in the workspace header that lce_check_error turns into a status.  Rows with such a
+ *     label are left out of the loss, of n_valid and of the gradients.  No call aborts the
+ *     process or traps the device.
+ *   - Shape rules (LCE_ERR_UNSUPPORTED_SHAPE otherwise): N >= 0, V >= 1, d >= 8 with
+ *     d % 8 == 0, strip_V >= 128 with strip_V % 128 == 0, N, d, V, strip_V < 2^31.
+ *   - Determinism: for a fixed device, shape and strip_V, every output is bitwise identical from
+ *     run to run (no atomics take part in any sum; every reduction has a fixed order).
+ *   - Not thread-safe across host threads only for the tracing calls (lce_trace_*).
+ */
+#ifndef LCE_H
+#define LCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LCE_OK = 0,
+  LCE_ERR_INVALID_ARG = 1,        /* null or misaligned pointer, unknown enum value            */
+  LCE_ERR_UNSUPPORTED_SHAPE = 2,  /* a shape rule above is broken                              */
+  LCE_ERR_WORKSPACE_TOO_SMALL = 3,/* ws_bytes < lce_workspace_size(...)                       */
+  LCE_ERR_LABEL_OUT_OF_RANGE = 4, /* device found a label outside [0, V) and != ignore_index   */
+  LCE_ERR_CUDA = 5,               /* a CUDA runtime call or a kernel launch failed             */
+  LCE_ERR_TIMEOUT = 6,            /* a kernel-side wait gave up (the kernel returned early)    */
+  LCE_ERR_UNSUPPORTED_DEVICE = 7  /* current device is not compute capability 10.3 (sm_103a)   */
+} lce_status_t;
+
+typedef enum { LCE_REDUCTION_MEAN = 0, LCE_REDUCTION_SUM = 1 } lce_reduction_t;
+typedef enum { LCE_BF16 = 0, LCE_F32 = 1 } lce_dtype_t;
+
+/*
+ * Bytes of device workspace that lce_forward and lce_backward need for these sizes; 0 when the
+ * arguments break a shape rule.  It grows as O(N * min(strip_V, V)) and never with V beyond the
+ * strip: this is the closed-form per-call budget that can be checked before launch
+ * ("Flattening Every Memory Peak", sections 3.5 and 6: the per-rank budget is fixed by the launch
+ * configuration).  Layout: a 256-byte header (error flags) followed by the larger of the
+ * forward region (running state, target logits, per-tile partial states of one strip) and the
+ * backward region (one strip of the logit gradient, N x strip_V elements of the input dtype).
+ */
+size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dtype);
+
+/*
+ * Forward.  Visits the vocabulary in strips of strip_V columns; for each strip it forms the
+ * logit tiles on the tensor cores, folds them into the running per-token state in the GEMM
+ * epilogue and drops them.  Writes
+ *   loss    : device fp32 scalar (MEAN over valid rows; NaN when n_valid == 0.  SUM: the sum)
+ *   lse     : device fp32 [N], log-sum-exp of every row (ignored rows included)
+ *   n_valid : device int64 scalar, number of rows whose label is in [0, V)
+ * ignore_index is any int64 value (conventionally -100).  Clears the workspace error flags.
+ */
+lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels,
+                         int64_t N, int64_t d, int64_t V, int64_t ignore_index, int64_t strip_V,
+                         lce_reduction_t reduction, lce_dtype_t dtype,
+                         float* loss, float* lse, int64_t* n_valid,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Backward from the saved per-token lse and n_valid (outputs of lce_forward on the same H, W,
+ * labels) and the incoming gradient dloss (device fp32 scalar).  For each strip it recomputes
+ * the logits, forms G = scale * (softmax - onehot) in the epilogue (scale = dloss / n_valid for
+ * MEAN, dloss for SUM) into one strip of workspace, then accumulates dH += G_s W_s and writes
+ * dW_s = G_s^T H on the tensor cores.  Writes dH (device fp32 [N x d], overwritten) and dW
+ * (device fp32 [V x d], overwritten).  dW rows are each written exactly once (deterministic).
+ */
+lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels,
+                          const float* lse, const int64_t* n_valid, const float* dloss,
+                          int64_t N, int64_t d, int64_t V, int64_t ignore_index, int64_t strip_V,
+                          lce_reduction_t reduction, lce_dtype_t dtype,
+                          float* dH, float* dW,
+                          void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises stream, then reads the workspace error flags written by the device:
+ * LCE_ERR_TIMEOUT, else LCE_ERR_LABEL_OUT_OF_RANGE, else LCE_OK (LCE_ERR_CUDA if the copy or the
+ * synchronisation itself fails).
+ */
+lce_status_t lce_check_error(const void* workspace, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* lce_status_string(lce_status_t status);
+
+/*
+ * Number of kernels this library has launched in this process so far (all entry points, all
+ * threads).  Used to count device launches inside a timed region.
+ */
+int64_t lce_launch_count(void);
+
+/*
+ * Optional launch tracing for profiling.  Between lce_trace_begin and lce_trace_end, every
+ * kernel launch made by lce_forward / lce_backward on the calling thread is bracketed by
+ * cudaEventRecord(start_events[k]) / cudaEventRecord(stop_events[k]) on its stream and tagged
+ * kernel_ids[k] (see lce_kernel_name), for k = 0 .. capacity-1; further launches are not
+ * recorded.  The events are caller-owned cudaEvent_t handles created with timing enabled.
+ * lce_trace_end returns the number of launches recorded.  Not thread-safe.
+ */
+lce_status_t lce_trace_begin(void* const* start_events, void* const* stop_events,
+                             int32_t* kernel_ids, int32_t capacity);
+int32_t lce_trace_end(void);
+
+/* Name of a traced kernel id ("tc_fwd_lse", "tc_bwd_grad", "tc_dh", "tc_dw", ...); NULL if unknown. */
+const char* lce_kernel_name(int32_t kernel_id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCE_H */

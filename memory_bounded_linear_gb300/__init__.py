@@ -13,3 +13,13 @@ def full_logits_bytes(tokens: int, vocab: int, bytes_per_element: int = 4) -> in
     """Bytes a materialised fp32 logits tensor would take: tokens x vocab x 4 (the memory this
     operator avoids)."""
     return int(tokens) * int(vocab) * int(bytes_per_element)
+
+
+def __getattr__(name):
+    # The binding is imported lazily so that host-only users (input recipes, sizes) do not need
+    # torch.cuda; it never falls back to anything when the library is missing.
+    if name in ("lce_workspace_size", "lce_forward", "lce_backward", "lce_check_error",
+                "lce_launch_count", "linear_cross_entropy", "LinearCrossEntropy"):
+        from . import api
+        return getattr(api, name)
+    raise AttributeError(name)

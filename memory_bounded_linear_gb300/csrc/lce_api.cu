@@ -1,0 +1,299 @@
+// C ABI of the memory-bounded linear cross-entropy library (declared in include/lce.h):
+// argument validation, workspace layout, the strip loop, launch counting and launch tracing.
+// Every compute step runs in the kernels of lce_tc.cu / lce_simt.cu / lce_reduce.cu.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "lce.h"
+#include "lce_internal.h"
+
+namespace lce {
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+  int bn;           // logit tile width of the engine
+  int64_t w;        // effective strip width min(strip_V, V)
+  int64_t ldg;      // row stride of the strip gradient workspace (elements)
+  int tiles;        // logit tiles per full strip
+  size_t off_run, off_tgt, off_part, off_g;
+  size_t total;
+};
+
+bool shape_ok(int64_t N, int64_t d, int64_t V, int64_t strip_V) {
+  if (N < 0 || N > kMaxDim) return false;
+  if (V < 1 || V > kMaxDim) return false;
+  if (d < 8 || d % 8 != 0 || d > kMaxDim) return false;
+  if (strip_V < 128 || strip_V % 128 != 0 || strip_V > kMaxDim) return false;
+  return true;
+}
+
+bool make_layout(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dt, Layout* L) {
+  if (!shape_ok(N, d, V, strip_V)) return false;
+  if (dt != LCE_BF16 && dt != LCE_F32) return false;
+  L->bn = (dt == LCE_BF16) ? TC_BN : SIMT_BN;
+  L->w = std::min(strip_V, V);
+  L->ldg = (L->w + L->bn - 1) / L->bn * L->bn;
+  L->tiles = static_cast<int>((L->w + L->bn - 1) / L->bn);
+  const size_t n = static_cast<size_t>(N);
+  const size_t elt = (dt == LCE_BF16) ? 2 : 4;
+  L->off_run = WS_HEADER_BYTES;
+  L->off_tgt = L->off_run + align256(n * sizeof(float2));
+  L->off_part = L->off_tgt + align256(n * sizeof(float));
+  const size_t fwd_end = L->off_part + align256(static_cast<size_t>(L->tiles) * n * sizeof(float2));
+  L->off_g = WS_HEADER_BYTES;
+  const size_t bwd_end = L->off_g + align256(n * static_cast<size_t>(L->ldg) * elt);
+  L->total = std::max(fwd_end, bwd_end);
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// --------------------------------------------------------------------------- device checks
+int g_sms[64];
+signed char g_dev_ok[64];  // 0 unknown, 1 ok, -1 not sm_103
+
+lce_status_t check_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LCE_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return LCE_ERR_UNSUPPORTED_DEVICE;
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return LCE_ERR_CUDA;
+    g_sms[dev] = sms;
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_dev_ok[dev] < 0) return LCE_ERR_UNSUPPORTED_DEVICE;
+  *num_sms = g_sms[dev];
+  return LCE_OK;
+}
+
+// --------------------------------------------------------------------------- launch bookkeeping
+std::atomic<int64_t> g_launches{0};
+
+struct Trace {
+  void* const* start = nullptr;
+  void* const* stop = nullptr;
+  int32_t* ids = nullptr;
+  int32_t cap = 0;
+  int32_t n = 0;
+  bool active = false;
+};
+Trace g_trace;
+
+template <typename F>
+cudaError_t traced(int kid, cudaStream_t stream, F&& launch) {
+  const bool rec = g_trace.active && g_trace.n < g_trace.cap;
+  if (rec) {
+    cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(g_trace.start[g_trace.n]), stream);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = launch();
+  if (e != cudaSuccess) return e;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (rec) {
+    e = cudaEventRecord(static_cast<cudaEvent_t>(g_trace.stop[g_trace.n]), stream);
+    if (e != cudaSuccess) return e;
+    g_trace.ids[g_trace.n] = kid;
+    ++g_trace.n;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t strip_gemm(const StripArgs& a, lce_dtype_t dt, cudaStream_t stream, int num_sms) {
+  if (dt == LCE_BF16) {
+    static const int kid[4] = {K_TC_FWD, K_TC_BWD_G, K_TC_DH, K_TC_DW};
+    return traced(kid[a.mode], stream, [&] { return tc_strip_gemm(a, stream, num_sms); });
+  }
+  static const int kid[4] = {K_SIMT_FWD, K_SIMT_BWD_G, K_SIMT_DH, K_SIMT_DW};
+  return traced(kid[a.mode], stream, [&] { return simt_strip_gemm(a, stream); });
+}
+
+lce_status_t common_checks(const void* H, const void* W, const int64_t* labels, int64_t N,
+                           int64_t d, int64_t V, int64_t strip_V, lce_reduction_t red,
+                           lce_dtype_t dt, const void* ws, size_t ws_bytes, Layout* L) {
+  if (red != LCE_REDUCTION_MEAN && red != LCE_REDUCTION_SUM) return LCE_ERR_INVALID_ARG;
+  if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_INVALID_ARG;
+  // H and labels may be null only when there is no token
+  if (!W || !ws || (N > 0 && (!H || !labels))) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(H) || !aligned16(W) || !aligned16(labels) || !aligned16(ws))
+    return LCE_ERR_INVALID_ARG;
+  if (!make_layout(N, d, V, strip_V, dt, L)) return LCE_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < L->total) return LCE_ERR_WORKSPACE_TOO_SMALL;
+  return LCE_OK;
+}
+
+}  // namespace
+}  // namespace lce
+
+using namespace lce;
+
+extern "C" {
+
+size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dtype) {
+  Layout L;
+  if (!make_layout(N, d, V, strip_V, dtype, &L)) return 0;
+  return L.total;
+}
+
+lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels, int64_t N, int64_t d,
+                         int64_t V, int64_t ignore_index, int64_t strip_V, lce_reduction_t reduction,
+                         lce_dtype_t dtype, float* loss, float* lse, int64_t* n_valid,
+                         void* workspace, size_t ws_bytes, void* stream_) {
+  Layout L;
+  lce_status_t st = common_checks(H, W, labels, N, d, V, strip_V, reduction, dtype, workspace,
+                                  ws_bytes, &L);
+  if (st != LCE_OK) return st;
+  if (!loss || !n_valid || (N > 0 && !lse)) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(lse)) return LCE_ERR_INVALID_ARG;
+  int num_sms = 0;
+  if ((st = check_device(&num_sms)) != LCE_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+  char* ws = static_cast<char*>(workspace);
+  unsigned* err = reinterpret_cast<unsigned*>(ws);
+  float2* run = reinterpret_cast<float2*>(ws + L.off_run);
+  float* tgt = reinterpret_cast<float*>(ws + L.off_tgt);
+  float2* part = reinterpret_cast<float2*>(ws + L.off_part);
+  if (cudaMemsetAsync(ws, 0, WS_HEADER_BYTES, stream) != cudaSuccess) return LCE_ERR_CUDA;
+
+  if (N > 0) {
+    for (int64_t col0 = 0, s = 0; col0 < V; col0 += strip_V, ++s) {
+      StripArgs a{};
+      a.mode = MODE_FWD_LSE;
+      a.col0 = static_cast<int>(col0);
+      a.strip_cols = static_cast<int>(std::min(strip_V, V - col0));
+      a.H = H; a.W = W; a.d = d; a.N = N; a.V = V;
+      a.part = part; a.tgt = tgt;
+      a.labels = labels; a.ignore_index = ignore_index;
+      a.err = err; a.first_strip = (s == 0);
+      if (strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;
+      const int tiles = (a.strip_cols + L.bn - 1) / L.bn;
+      if (traced(K_COMBINE, stream, [&] {
+            return launch_combine(part, tiles, N, run, s == 0, stream);
+          }) != cudaSuccess)
+        return LCE_ERR_CUDA;
+    }
+  }
+  if (traced(K_FINALIZE, stream, [&] {
+        return launch_finalize(run, tgt, labels, N, V, ignore_index, reduction, loss, lse, n_valid,
+                               err, stream);
+      }) != cudaSuccess)
+    return LCE_ERR_CUDA;
+  return LCE_OK;
+}
+
+lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, const float* lse,
+                          const int64_t* n_valid, const float* dloss, int64_t N, int64_t d, int64_t V,
+                          int64_t ignore_index, int64_t strip_V, lce_reduction_t reduction,
+                          lce_dtype_t dtype, float* dH, float* dW, void* workspace,
+                          size_t ws_bytes, void* stream_) {
+  Layout L;
+  lce_status_t st = common_checks(H, W, labels, N, d, V, strip_V, reduction, dtype, workspace,
+                                  ws_bytes, &L);
+  if (st != LCE_OK) return st;
+  if (!n_valid || !dloss || !dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(lse) || !aligned16(dH) || !aligned16(dW)) return LCE_ERR_INVALID_ARG;
+  int num_sms = 0;
+  if ((st = check_device(&num_sms)) != LCE_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+  char* ws = static_cast<char*>(workspace);
+  unsigned* err = reinterpret_cast<unsigned*>(ws);
+  void* G = ws + L.off_g;
+  if (N == 0) {
+    // no token: every logit-gradient row is absent, so dW = 0 (dH has no rows)
+    if (cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * d * sizeof(float), stream) != cudaSuccess)
+      return LCE_ERR_CUDA;
+    return LCE_OK;
+  }
+  for (int64_t col0 = 0, s = 0; col0 < V; col0 += strip_V, ++s) {
+    StripArgs a{};
+    a.col0 = static_cast<int>(col0);
+    a.strip_cols = static_cast<int>(std::min(strip_V, V - col0));
+    a.H = H; a.W = W; a.d = d; a.N = N; a.V = V;
+    a.G = G; a.ldg = L.ldg;
+    a.labels = labels; a.ignore_index = ignore_index;
+    a.lse = lse; a.dloss = dloss; a.n_valid = n_valid; a.reduction = reduction;
+    a.err = err; a.first_strip = (s == 0);
+
+    a.mode = MODE_BWD_G;
+    if (strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;
+
+    a.mode = MODE_DH;
+    a.C = dH; a.ldc = d; a.accumulate = (s > 0); a.c_rows = static_cast<int>(N);
+    a.c_cols = static_cast<int>(d);
+    if (strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;
+
+    a.mode = MODE_DW;
+    a.C = dW + static_cast<size_t>(col0) * d; a.ldc = d; a.accumulate = 0;
+    a.c_rows = a.strip_cols; a.c_cols = static_cast<int>(d);
+    if (strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;
+  }
+  return LCE_OK;
+}
+
+lce_status_t lce_check_error(const void* workspace, void* stream_) {
+  if (!workspace) return LCE_ERR_INVALID_ARG;
+  unsigned flags = 0;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (cudaMemcpyAsync(&flags, workspace, sizeof(flags), cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return LCE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return LCE_ERR_CUDA;
+  if (flags & ERR_TIMEOUT) return LCE_ERR_TIMEOUT;
+  if (flags & ERR_LABEL) return LCE_ERR_LABEL_OUT_OF_RANGE;
+  return LCE_OK;
+}
+
+const char* lce_status_string(lce_status_t s) {
+  switch (s) {
+    case LCE_OK: return "ok";
+    case LCE_ERR_INVALID_ARG: return "invalid argument";
+    case LCE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case LCE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case LCE_ERR_LABEL_OUT_OF_RANGE: return "label out of range";
+    case LCE_ERR_CUDA: return "CUDA error";
+    case LCE_ERR_TIMEOUT: return "kernel wait timed out";
+    case LCE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+  }
+  return "unknown status";
+}
+
+int64_t lce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+lce_status_t lce_trace_begin(void* const* start_events, void* const* stop_events,
+                             int32_t* kernel_ids, int32_t capacity) {
+  if (capacity < 0 || (capacity > 0 && (!start_events || !stop_events || !kernel_ids)))
+    return LCE_ERR_INVALID_ARG;
+  g_trace.start = start_events;
+  g_trace.stop = stop_events;
+  g_trace.ids = kernel_ids;
+  g_trace.cap = capacity;
+  g_trace.n = 0;
+  g_trace.active = true;
+  return LCE_OK;
+}
+
+int32_t lce_trace_end(void) {
+  g_trace.active = false;
+  return g_trace.n;
+}
+
+const char* lce_kernel_name(int32_t id) {
+  static const char* names[K_NUM] = {"tc_fwd_lse", "tc_bwd_grad", "tc_dh", "tc_dw",
+                                     "simt_fwd_lse", "simt_bwd_grad", "simt_dh", "simt_dw",
+                                     "combine", "finalize"};
+  return (id >= 0 && id < K_NUM) ? names[id] : nullptr;
+}
+
+}  // extern "C"

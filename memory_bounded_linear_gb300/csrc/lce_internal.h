@@ -1,0 +1,68 @@
+// Internal interfaces between the C-ABI host code (lce_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lce {
+
+// Error-flag bits kept in the first word of the workspace header.
+constexpr unsigned ERR_LABEL = 1u;     // a label outside [0, V) that is not ignore_index
+constexpr unsigned ERR_TIMEOUT = 2u;   // a kernel-side wait ran out of time
+
+constexpr size_t WS_HEADER_BYTES = 256;
+
+// The four epilogues of the strip GEMM engine.
+enum Mode : int {
+  MODE_FWD_LSE = 0,  // Z tile = H W_s^T; epilogue folds it into per-(row, tile) (max, sum-exp)
+  MODE_BWD_G = 1,    // Z tile recomputed; epilogue writes G = scale (softmax - onehot)
+  MODE_DH = 2,       // dH (+)= G_s W_s
+  MODE_DW = 3,       // dW_s = G_s^T H
+};
+
+// Kernel ids reported by the launch tracer.
+enum KernelId : int {
+  K_TC_FWD = 0, K_TC_BWD_G = 1, K_TC_DH = 2, K_TC_DW = 3,
+  K_SIMT_FWD = 4, K_SIMT_BWD_G = 5, K_SIMT_DH = 6, K_SIMT_DW = 7,
+  K_COMBINE = 8, K_FINALIZE = 9, K_NUM = 10
+};
+
+// Arguments of one strip-GEMM launch (both the tensor-core and the fp32 CUDA-core engines).
+// GEMM view: C[M x Ncols] = A[M x K] * B[Ncols x K]^T.
+struct StripArgs {
+  int mode;
+  int M, Ncols, K;            // GEMM extents
+  int col0;                   // first vocabulary column of the strip (W row offset)
+  int strip_cols;             // columns of this strip (<= strip_V)
+  // operands (device pointers)
+  const void* H; const void* W; int64_t d, N, V;
+  void* G; int64_t ldg;       // strip gradient workspace, row stride ldg elements
+  // forward epilogue
+  float2* part;               // [tiles_n][N] per-(tile, row) (max, sum-exp)
+  float* tgt;                 // [N] target logit
+  // backward epilogue
+  const int64_t* labels; int64_t ignore_index;
+  const float* lse; const float* dloss; const int64_t* n_valid; int reduction;
+  // dH / dW epilogue
+  float* C; int64_t ldc; int accumulate; int c_rows; int c_cols;
+  unsigned* err;
+  int first_strip;
+};
+
+// Tile widths of the two engines (columns of a logit tile).
+constexpr int TC_BN = 256;
+constexpr int SIMT_BN = 64;
+
+// Tensor-core (tcgen05) engine, bf16 operands: lce_tc.cu
+cudaError_t tc_strip_gemm(const StripArgs& a, cudaStream_t stream, int num_sms);
+// CUDA-core engine, fp32 operands (exact FFMA): lce_simt.cu
+cudaError_t simt_strip_gemm(const StripArgs& a, cudaStream_t stream);
+// Reductions: lce_reduce.cu
+cudaError_t launch_combine(const float2* part, int tiles, int64_t N, float2* run, int first,
+                           cudaStream_t stream);
+cudaError_t launch_finalize(const float2* run, const float* tgt, const int64_t* labels,
+                            int64_t N, int64_t V, int64_t ignore_index, int reduction,
+                            float* loss, float* lse, int64_t* n_valid, unsigned* err,
+                            cudaStream_t stream);
+
+}  // namespace lce

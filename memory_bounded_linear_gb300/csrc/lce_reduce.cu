@@ -1,0 +1,104 @@
+// Per-token state reductions of the forward pass.
+//
+// combine:  folds the per-(tile, row) (max, sum-exp) partials of one vocabulary strip, in tile
+//           order, into the running per-token state (m, s):
+//             (m, s) (+) (m', s') = (M, s e^(m - M) + s' e^(m' - M)),  M = max(m, m')
+//           ("Flattening Every Memory Peak", section 3.2: each strip is folded into a running
+//           per-token state and released).  One thread per token, coalesced over tokens.
+// finalize: lse_i = m_i + log s_i for every row; per-token loss lse_i - t_i on valid rows; the
+//           sum over rows in a fixed order in fp64 (one block, fixed per-thread strides and a
+//           fixed tree), n_valid, and the label-range check.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "lce_internal.h"
+
+namespace lce {
+namespace {
+
+__device__ __forceinline__ float2 fold(float2 a, float2 b) {
+  const float M = fmaxf(a.x, b.x);
+  if (M == -INFINITY) return make_float2(-INFINITY, 0.f);
+  return make_float2(M, a.y * expf(a.x - M) + b.y * expf(b.x - M));
+}
+
+__global__ void combine_kernel(const float2* __restrict__ part, int tiles, int64_t N,
+                               float2* __restrict__ run, int first) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  float2 st = first ? make_float2(-INFINITY, 0.f) : run[i];
+  for (int t = 0; t < tiles; ++t) st = fold(st, part[static_cast<size_t>(t) * N + i]);
+  run[i] = st;
+}
+
+constexpr int FIN_THREADS = 1024;
+
+__global__ void __launch_bounds__(FIN_THREADS)
+    finalize_kernel(const float2* __restrict__ run, const float* __restrict__ tgt,
+                    const int64_t* __restrict__ labels, int64_t N, int64_t V, int64_t ignore_index,
+                    int reduction, float* loss, float* lse, int64_t* n_valid, unsigned* err) {
+  __shared__ double ssum[FIN_THREADS];
+  __shared__ long long scnt[FIN_THREADS];
+  __shared__ int sbad;
+  if (threadIdx.x == 0) sbad = 0;
+  __syncthreads();
+  double acc = 0.0;
+  long long cnt = 0;
+  int bad = 0;
+  for (int64_t i = threadIdx.x; i < N; i += FIN_THREADS) {
+    const float2 st = run[i];
+    const float l = st.x + logf(st.y);
+    lse[i] = l;
+    const int64_t y = labels[i];
+    const bool in_range = (y >= 0) && (y < V);
+    if (y != ignore_index && in_range) {
+      acc += static_cast<double>(l) - static_cast<double>(tgt[i]);
+      ++cnt;
+    } else if (y != ignore_index) {
+      bad = 1;
+    }
+  }
+  ssum[threadIdx.x] = acc;
+  scnt[threadIdx.x] = cnt;
+  if (bad) sbad = 1;
+  __syncthreads();
+  for (int w = FIN_THREADS / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      ssum[threadIdx.x] += ssum[threadIdx.x + w];
+      scnt[threadIdx.x] += scnt[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double total = ssum[0];
+    const long long nv = scnt[0];
+    if (reduction == 0)
+      *loss = nv > 0 ? static_cast<float>(total / static_cast<double>(nv)) : nanf("");
+    else
+      *loss = static_cast<float>(total);
+    *n_valid = nv;
+    if (sbad) atomicOr(err, ERR_LABEL);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float2* part, int tiles, int64_t N, float2* run, int first,
+                           cudaStream_t stream) {
+  if (N == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (N + threads - 1) / threads;
+  combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(part, tiles, N, run, first);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float2* run, const float* tgt, const int64_t* labels, int64_t N,
+                            int64_t V, int64_t ignore_index, int reduction, float* loss, float* lse,
+                            int64_t* n_valid, unsigned* err, cudaStream_t stream) {
+  finalize_kernel<<<1, FIN_THREADS, 0, stream>>>(run, tgt, labels, N, V, ignore_index, reduction,
+                                                 loss, lse, n_valid, err);
+  return cudaGetLastError();
+}
+
+}  // namespace lce

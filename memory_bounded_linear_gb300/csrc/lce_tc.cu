@@ -1,0 +1,537 @@
+// Tensor-core strip GEMM engine for bf16 operands on sm_103a (tcgen05 + TMEM + TMA).
+//
+// One persistent, warp-specialised kernel per epilogue mode:
+//   warp 0      TMA producer: streams A and B k-blocks (64 bf16 = one 128-byte swizzle span)
+//               into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and one elected
+//               lane issues tcgen05.mma (M=128, N=256, K=16) into the accumulator of the tile;
+//   warps 2..5  epilogue: each thread owns one accumulator row (TMEM lane) and reads its 256
+//               columns 32 at a time with tcgen05.ld, so every per-row reduction of the tile
+//               (max, sum of exp, target gather) is thread-local -- no shuffles are needed.
+// While the epilogue drains one accumulator the MMA warp fills the other.
+//
+// GEMM view: C[M x Ncols] = A[M x K] B[Ncols x K]^T.  Operand layouts per mode:
+//   FWD_LSE, BWD_G  A = H   [N x d] K-major    B = W strip [w x d] K-major
+//   DH              A = G_s [N x w] K-major    B = W strip [w x d] MN-major (d contiguous)
+//   DW              A = G_s^T      MN-major    B = H [N x d]       MN-major
+// TMA zero-fills every box element outside the tensor, so ragged M, N and K edges contribute 0
+// to the products; the epilogues mask the columns beyond the strip / vocabulary.
+//
+// "Flattening Every Memory Peak in Long-Context MoE Training", section 3.2 / appendix C: each
+// logit strip is folded into a running per-token state and released; backward recomputes the
+// strip and its gradient.  Here a strip's logits only ever live in TMEM.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "lce_internal.h"
+#include "ptx.cuh"
+
+namespace lce {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = TC_BN;  // 256
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_BYTES = BN * BK * 2;        // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MN_BOX_BYTES = 64 * BK * 2;   // one 64(MN) x 64(K) box of an MN-major operand
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int CTL_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + CTL_BYTES;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // a wait longer than 2 s is treated as a hang
+constexpr int RASTER_GROUP = 16;                   // row tiles per rasterisation group
+
+struct Ctl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Ctl) <= CTL_BYTES, "control block too large");
+
+struct KParams {
+  int M, Ncols, K;
+  int tiles_m, tiles_n, num_tiles, nkb;
+  int b_off;        // FWD/BWD: W row of the strip start; DH: W row (K coordinate) of the strip start
+  int strip_cols;   // FWD/BWD: valid columns of the strip
+  int col0;         // first vocabulary column of the strip
+  float2* part;
+  float* tgt;
+  const int64_t* labels;
+  int64_t V, ignore_index;
+  const float* lse;
+  const float* dloss;
+  const int64_t* n_valid;
+  int reduction;
+  __nv_bfloat16* G;
+  int64_t ldg;
+  float* C;
+  int64_t ldc;
+  int accumulate, c_rows, c_cols;
+  unsigned* err;
+  int first_strip;
+};
+
+// Bounded wait on an mbarrier phase.  Gives up after WAIT_LIMIT_NS (or at once when another role
+// already gave up), raising the CTA's abort flag and the workspace timeout bit.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned* err) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (*abort_flag) return false;
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::globaltimer() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      atomicOr(err, ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Wait on a barrier regardless of the abort flag, for at most `limit_ns` (used while draining).
+__device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if (ptx::globaltimer() - t0 > limit_ns) return;
+}
+
+// Grouped rasterisation: RASTER_GROUP row tiles sweep the column tiles together, so the tiles
+// resident at one time share a few A row-blocks and B column-blocks through L2.
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int per_group = RASTER_GROUP * tiles_n;
+  const int group = tile / per_group;
+  const int first_m = group * RASTER_GROUP;
+  const int gm = min(tiles_m - first_m, RASTER_GROUP);
+  const int r = tile - group * per_group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_base, int k16) {
+  // K-major, 128B swizzle: rows of 128 bytes, 8-row swizzle atoms 1024 bytes apart; the k-th
+  // 16-element slice starts 32 bytes further into the row.
+  return ptx::sw128_desc(tile_base + k16 * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_base, int k16) {
+  // MN-major, 128B swizzle: each 64-wide MN box holds BK rows (one per k) of 128 bytes; boxes
+  // are MN_BOX_BYTES apart (leading byte offset), groups of 8 k-rows 1024 bytes apart (stride
+  // byte offset); the k-th 16-row slice starts 16 * 128 bytes further.
+  return ptx::sw128_desc(tile_base + k16 * 16 * 128, MN_BOX_BYTES, 1024);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_strip_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const KParams p) {
+  constexpr bool A_MN = (MODE == MODE_DW);
+  constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
+  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;  // 128B-swizzled tiles need 1024B alignment
+  uint8_t* smem = smem_raw + (base - raw_addr);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  volatile int* abort_flag = &ctl->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->tfull[b]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->tempty[b]), 4);  // one arrival per epilogue warp
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
+    ctl->abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmB);
+      bool ok = true;
+      int stage = 0;
+      uint32_t ph = 0;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int tm, tn;
+        tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          const uint32_t empty = ptx::smem_addr(&ctl->empty[stage]);
+          const uint32_t full = ptx::smem_addr(&ctl->full[stage]);
+          if (!wait_bar(empty, ph ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          const uint32_t sa = base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+          if (A_MN) {
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c)
+              ptx::tma_load_2d(sa + c * MN_BOX_BYTES, &tmA, tm * BM + c * 64, kb * BK, full);
+          } else {
+            ptx::tma_load_2d(sa, &tmA, kb * BK, tm * BM, full);
+          }
+          if (B_MN) {
+            const int krow = (MODE == MODE_DH ? p.b_off : 0) + kb * BK;
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              ptx::tma_load_2d(sb + c * MN_BOX_BYTES, &tmB, tn * BN + c * 64, krow, full);
+          } else {
+            ptx::tma_load_2d(sb, &tmB, kb * BK, p.b_off + tn * BN, full);
+          }
+          if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // Let copies already in flight land before the CTA can exit.
+        const uint64_t t0 = ptx::globaltimer();
+        while (ptx::globaltimer() - t0 < 2000000ull) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t aph = 0;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        if (!wait_bar(ptx::smem_addr(&ctl->tempty[acc]), aph ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          if (!wait_bar(ptx::smem_addr(&ctl->full[stage]), ph, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = A_MN ? desc_mnmajor(sa, k) : desc_kmajor(sa, k);
+            const uint64_t bd = B_MN ? desc_mnmajor(sb, k) : desc_kmajor(sb, k);
+            ptx::tc_mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::tc_commit(ptx::smem_addr(&ctl->empty[stage]));  // frees the stage when read
+          if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::tc_commit(ptx::smem_addr(&ctl->tfull[acc]));  // accumulator ready for the epilogue
+        acc ^= 1;
+        if (acc == 0) aph ^= 1u;
+      }
+      if (!ok) {
+        // Make sure no MMA is still writing TMEM before it is released.
+        ptx::tc_commit(ptx::smem_addr(&ctl->drain));
+        wait_bar_drain(ptx::smem_addr(&ctl->drain), 0, 100000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;          // TMEM lane quadrant this warp may access
+    const int r_in = q * 32 + lane;  // accumulator row owned by this thread
+    float scale_valid = 0.f;
+    if (MODE == MODE_BWD_G) {
+      const float dl = *p.dloss;
+      scale_valid = (p.reduction == 0) ? dl / static_cast<float>(*p.n_valid) : dl;
+    }
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      int tm, tn;
+      tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+      const uint32_t tfull = ptx::smem_addr(&ctl->tfull[acc]);
+      const uint32_t tempty = ptx::smem_addr(&ctl->tempty[acc]);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+
+      if (MODE == MODE_FWD_LSE || MODE == MODE_BWD_G) {
+        const int row = tm * BM + r_in;
+        const bool row_ok = row < p.M;
+        const int tcol0 = tn * BN;
+        const int ncols = min(BN, p.strip_cols - tcol0);  // valid columns of this tile (>= 1)
+        const int64_t y = row_ok ? p.labels[row] : p.ignore_index;
+        const bool label_ok = (y != p.ignore_index) && (y >= 0) && (y < p.V);
+        const int64_t trel = y - static_cast<int64_t>(p.col0 + tcol0);
+        const int tloc = (label_ok && trel >= 0 && trel < ncols) ? static_cast<int>(trel) : -1;
+
+        if (MODE == MODE_FWD_LSE) {
+          float m = -INFINITY, s = 0.f, t = 0.f;
+          if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            if (c * 32 >= ncols) break;  // same for every thread of the CTA
+            float v[32];
+            ptx::tmem_load32(tbase + c * 32, v);
+            const int lim = ncols - c * 32;
+            if (lim < 32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j >= lim) v[j] = -INFINITY;
+            }
+            if (static_cast<unsigned>(tloc - c * 32) < 32u) {
+              const int jt = tloc - c * 32;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == jt) t = v[j];
+            }
+            float cm = v[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) cm = fmaxf(cm, v[j]);
+            const float mn = fmaxf(m, cm);
+            const float nml = -mn * LOG2E;
+            float cs = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cs += exp2f(fmaf(v[j], LOG2E, nml));
+            s = s * exp2f(fmaf(m, LOG2E, nml)) + cs;
+            m = mn;
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(tempty);
+          if (row_ok) {
+            p.part[static_cast<size_t>(tn) * p.M + row] = make_float2(m, s);
+            if (tloc >= 0) p.tgt[row] = t;
+          }
+        } else {
+          // MODE_BWD_G: G = scale * (exp(Z - lse) - onehot) -> bf16 strip workspace
+          if (row_ok && !label_ok && y != p.ignore_index && p.first_strip && tn == 0)
+            atomicOr(p.err, ERR_LABEL);
+          const float scale = label_ok ? scale_valid : 0.f;
+          const float nl = label_ok ? -p.lse[row] * LOG2E : 0.f;
+          __nv_bfloat16* grow = p.G + static_cast<size_t>(row) * p.ldg + tcol0;
+          if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t packed[16];
+            if (c * 32 < ncols) {
+              float v[32];
+              ptx::tmem_load32(tbase + c * 32, v);
+              const int lim = ncols - c * 32;
+              const int jt = tloc - c * 32;
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                float g0 = (j < lim) ? scale * exp2f(fmaf(v[j], LOG2E, nl)) : 0.f;
+                float g1 = (j + 1 < lim) ? scale * exp2f(fmaf(v[j + 1], LOG2E, nl)) : 0.f;
+                if (j == jt) g0 -= scale;
+                if (j + 1 == jt) g1 -= scale;
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(g0, g1);
+                packed[j / 2] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) packed[j] = 0u;
+            }
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(grow + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                    packed[4 * i + 3]);
+            }
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(tempty);
+        }
+      } else {
+        // MODE_DH / MODE_DW: C (+)= accumulator, fp32
+        const int row = tm * BM + r_in;
+        const bool row_ok = row < p.c_rows;
+        float* crow = p.C + static_cast<size_t>(row) * p.ldc;
+        if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col = tn * BN + c * 32;
+          if (col >= p.c_cols) break;  // same for every thread of the CTA
+          float v[32];
+          ptx::tmem_load32(tbase + c * 32, v);
+          if (!row_ok) continue;
+          if (col + 32 <= p.c_cols) {
+            float4* dst = reinterpret_cast<float4*>(crow + col);
+            if (p.accumulate) {
+              float4 o[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o[i] = dst[i];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(o[i].x + v[4 * i], o[i].y + v[4 * i + 1],
+                                     o[i].z + v[4 * i + 2], o[i].w + v[4 * i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col + j < p.c_cols) crow[col + j] = (p.accumulate ? crow[col + j] : 0.f) + v[j];
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty);
+      }
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer x inner] array with `ld` elements per row,
+// box = [box_outer x box_inner], 128-byte swizzle, zero fill outside the array.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+              uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KParams& p, int grid,
+                        cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tc_strip_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  tc_strip_kernel<MODE><<<grid, THREADS, SMEM_BYTES, stream>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) {
+  KParams p{};
+  CUtensorMap ma, mb;
+  bool ok = true;
+  switch (s.mode) {
+    case MODE_FWD_LSE:
+    case MODE_BWD_G:
+      p.M = static_cast<int>(s.N);
+      p.Ncols = s.strip_cols;
+      p.K = static_cast<int>(s.d);
+      p.b_off = s.col0;
+      ok = make_map(&ma, s.H, s.d, s.N, s.d, BK, BM) && make_map(&mb, s.W, s.d, s.V, s.d, BK, BN);
+      break;
+    case MODE_DH:
+      p.M = static_cast<int>(s.N);
+      p.Ncols = static_cast<int>(s.d);
+      p.K = s.strip_cols;
+      p.b_off = s.col0;
+      ok = make_map(&ma, s.G, s.ldg, s.N, s.ldg, BK, BM) && make_map(&mb, s.W, s.d, s.V, s.d, 64, BK);
+      break;
+    case MODE_DW:
+      p.M = s.strip_cols;
+      p.Ncols = static_cast<int>(s.d);
+      p.K = static_cast<int>(s.N);
+      p.b_off = 0;
+      ok = make_map(&ma, s.G, s.ldg, s.N, s.ldg, 64, BK) && make_map(&mb, s.H, s.d, s.N, s.d, 64, BK);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  p.tiles_m = (p.M + BM - 1) / BM;
+  p.tiles_n = (p.Ncols + BN - 1) / BN;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.nkb = (p.K + BK - 1) / BK;
+  if (p.num_tiles == 0 || p.nkb == 0) return cudaSuccess;
+  p.strip_cols = s.strip_cols;
+  p.col0 = s.col0;
+  p.part = s.part;
+  p.tgt = s.tgt;
+  p.labels = s.labels;
+  p.V = s.V;
+  p.ignore_index = s.ignore_index;
+  p.lse = s.lse;
+  p.dloss = s.dloss;
+  p.n_valid = s.n_valid;
+  p.reduction = s.reduction;
+  p.G = static_cast<__nv_bfloat16*>(s.G);
+  p.ldg = s.ldg;
+  p.C = s.C;
+  p.ldc = s.ldc;
+  p.accumulate = s.accumulate;
+  p.c_rows = s.c_rows;
+  p.c_cols = s.c_cols;
+  p.err = s.err;
+  p.first_strip = s.first_strip;
+  const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+  switch (s.mode) {
+    case MODE_FWD_LSE: return launch_mode<MODE_FWD_LSE>(ma, mb, p, grid, stream);
+    case MODE_BWD_G: return launch_mode<MODE_BWD_G>(ma, mb, p, grid, stream);
+    case MODE_DH: return launch_mode<MODE_DH>(ma, mb, p, grid, stream);
+    default: return launch_mode<MODE_DW>(ma, mb, p, grid, stream);
+  }
+}
+
+}  // namespace lce

@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI, no GPU needed: the library loads, exports every symbol that
+include/lce.h declares, sizes its workspace, and rejects bad arguments before launching anything
+(every call below returns from host validation; none reaches the CUDA runtime)."""
+
+import ctypes
+import os
+
+import pytest
+
+from memory_bounded_linear_gb300 import _lib
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        from memory_bounded_linear_gb300.csrc import build
+        build.build()
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _lib.header_symbols()
+    assert set(declared) >= {"lce_workspace_size", "lce_forward", "lce_backward",
+                             "lce_check_error", "lce_status_string"}
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(_lib._SIGNATURES) >= set(declared)
+
+
+def test_status_strings_and_kernel_names(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        s = lib.lce_status_string(code)
+        assert s and s != b"unknown status", name
+    assert lib.lce_status_string(99) == b"unknown status"
+    assert lib.lce_kernel_name(0) == b"tc_fwd_lse"
+    assert lib.lce_kernel_name(3) == b"tc_dw"
+    assert lib.lce_kernel_name(-1) is None and lib.lce_kernel_name(1000) is None
+
+
+def _ws(lib, N, d, V, s, dt=0):
+    return lib.lce_workspace_size(N, d, V, s, dt)
+
+
+def test_workspace_size_formula(lib):
+    # bf16: header + max(forward state, one strip of bf16 gradient rows padded to 256 columns)
+    N, d, V, s = 32768, 6144, 151552, 16384
+    g_bytes = N * 16384 * 2
+    assert _ws(lib, N, d, V, s) == 256 + g_bytes
+    # fp32 engine: 64-wide tiles, fp32 gradient strip
+    assert _ws(lib, 256, 256, 4096, 512, 1) == 256 + 256 * 512 * 4
+    # strip wider than V: the strip is V wide (padded to the tile width)
+    assert _ws(lib, 100, 64, 300, 4096) == 256 + max(
+        ((100 * 8 + 255) // 256 * 256) + ((100 * 4 + 255) // 256 * 256) + ((2 * 100 * 8 + 255) // 256 * 256),
+        (100 * 512 * 2 + 255) // 256 * 256)
+
+
+def test_workspace_is_bounded_by_strip_not_vocab(lib):
+    a = _ws(lib, 65536, 2048, 151936, 4096)
+    b = _ws(lib, 65536, 2048, 10 * 151936, 4096)
+    assert a == b
+    sweep = [_ws(lib, 65536, 2048, 151936, s) for s in (4096, 8192, 16384, 32768)]
+    assert all(x < y for x, y in zip(sweep, sweep[1:]))
+    assert sweep[-1] < 65536 * 151936 * 4 / 4   # well under the N x V fp32 logits
+
+
+@pytest.mark.parametrize("N,d,V,s", [(-1, 64, 100, 128), (10, 7, 100, 128), (10, 12, 100, 128),
+                                     (10, 64, 0, 128), (10, 64, 100, 64), (10, 64, 100, 200),
+                                     (1 << 31, 64, 100, 128)])
+def test_workspace_size_rejects_bad_shapes(lib, N, d, V, s):
+    assert _ws(lib, N, d, V, s) == 0
+
+
+class _Buf:
+    """Host memory that stands in for device pointers; validation fails before any access."""
+
+    def __init__(self, n=1 << 16):
+        self.raw = ctypes.create_string_buffer(n + 64)
+        self.addr = (ctypes.addressof(self.raw) + 63) // 64 * 64
+
+
+def _fwd(lib, H, W, y, N=16, d=64, V=300, s=128, red=0, dt=0, ws=None, wsb=1 << 20,
+         loss=None, lse=None, nv=None):
+    b = _Buf()
+    ws = b.addr if ws is None else ws
+    return lib.lce_forward(H, W, y, N, d, V, -100, s, red, dt,
+                           b.addr if loss is None else loss, b.addr if lse is None else lse,
+                           b.addr if nv is None else nv, ws, wsb, None)
+
+
+def test_forward_validation(lib):
+    b = _Buf()
+    p = b.addr
+    assert _fwd(lib, p, p, p, red=2) == 1                 # unknown reduction
+    assert _fwd(lib, p, p, p, dt=5) == 1                  # unknown dtype
+    assert _fwd(lib, p, None, p) == 1                     # null W
+    assert _fwd(lib, None, p, p) == 1                     # null H with N > 0
+    assert _fwd(lib, p + 4, p, p) == 1                    # misaligned H
+    assert _fwd(lib, p, p, p, d=12) == 2                  # d % 8 != 0
+    assert _fwd(lib, p, p, p, s=100) == 2                 # strip_V % 128 != 0
+    assert _fwd(lib, p, p, p, V=0) == 2
+    assert _fwd(lib, p, p, p, wsb=100) == 3               # workspace too small
+    assert _fwd(lib, p, p, p, lse=p + 8) == 1             # misaligned lse
+
+
+def test_backward_validation(lib):
+    b = _Buf()
+    p = b.addr
+    args = dict(N=16, d=64, V=300, s=128)
+
+    def bwd(H=p, W=p, y=p, lse=p, nv=p, dl=p, dH=p, dW=p, red=0, dt=0, wsb=1 << 20, **kw):
+        a = dict(args, **kw)
+        return lib.lce_backward(H, W, y, lse, nv, dl, a["N"], a["d"], a["V"], -100, a["s"], red, dt,
+                                dH, dW, p, wsb, None)
+
+    assert bwd(dl=None) == 1
+    assert bwd(dW=None) == 1
+    assert bwd(dH=p + 4) == 1
+    assert bwd(red=7) == 1
+    assert bwd(d=4) == 2
+    assert bwd(wsb=16) == 3
+
+
+def test_check_error_and_trace_argument_validation(lib):
+    assert lib.lce_check_error(None, None) == 1
+    assert lib.lce_trace_begin(None, None, None, 4) == 1
+    assert lib.lce_trace_begin(None, None, None, 0) == 0
+    assert lib.lce_trace_end() == 0
+    assert lib.lce_launch_count() >= 0

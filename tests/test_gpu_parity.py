@@ -1,0 +1,177 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle, element by element,
+on seeded inputs small enough for the oracle, spanning several tiles with ragged tails."""
+
+import numpy as np
+import pytest
+import torch
+
+from memory_bounded_linear_gb300 import api
+from memory_bounded_linear_gb300._lib import LceError
+from memory_bounded_linear_gb300.workloads import WORKLOADS, make_inputs
+
+from ._parity import assert_parity, parity_case, rel_fro, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+W2 = WORKLOADS["n4096-d2048-v151936"]
+W3 = WORKLOADS["n16384-d4096-v131072-ignore10"]
+W4 = WORKLOADS["n65536-d2048-v151936"]
+W5 = WORKLOADS["n32768-d6144-v151552-outliers"]
+WT = WORKLOADS["tiny-fp32"]
+
+
+def test_tiny_fp32_workload_full(cuda_lib):
+    parity_case(WT)
+
+
+@pytest.mark.parametrize("w", [
+    W2.with_sizes(N=300, d=136, V=1000, strip_V=384),      # ragged N, d (K tail), V, strips
+    W3.with_sizes(N=517, d=256, V=2048, strip_V=512),      # 10% ignored rows
+    W5.with_sizes(N=400, d=320, V=2500, strip_V=1024),     # outlier W rows, sum reduction
+    W2.with_sizes(N=256, d=1024, V=512, strip_V=256),      # long K loop, exact tiles
+    W2.with_sizes(N=129, d=64, V=257, strip_V=128),        # one past a tile in every direction
+    W4.with_sizes(N=1000, d=192, V=3001, strip_V=4096),    # one strip wider than V
+], ids=["ragged", "ignore10", "outliers-sum", "longK", "tile+1", "strip>V"])
+def test_bf16_reduced_workloads(cuda_lib, w):
+    parity_case(w)
+
+
+@pytest.mark.parametrize("w", [
+    WT.with_sizes(N=100, d=72, V=1000, strip_V=384),
+    WT.with_sizes(N=70, d=8, V=130, strip_V=128, reduction="sum"),
+], ids=["f32-ragged", "f32-min-d-sum"])
+def test_fp32_reduced(cuda_lib, w):
+    parity_case(w)
+
+
+@pytest.mark.parametrize("strip", [128, 256, 1024, 4096])
+def test_strip_width_invariance(cuda_lib, strip):
+    """Only the order changes with the strip width: every width matches one oracle result."""
+    w = W4.with_sizes(N=600, d=128, V=3001, strip_V=strip)
+    H, W, y = make_inputs(w, "cpu")
+    r = run_oracle(H, W, y, "mean")
+    g = run_gpu(H, W, y, strip, "mean")
+    assert_parity(g, r, "bf16")
+
+
+@pytest.mark.parametrize("dtype_name", ["bf16", "f32"])
+def test_edge_single_token_and_tiny_vocab(cuda_lib, dtype_name):
+    base = W2 if dtype_name == "bf16" else WT
+    for N, d, V in [(1, 8, 1), (1, 16, 2), (3, 8, 5), (130, 24, 1)]:
+        w = base.with_sizes(N=N, d=d, V=V, strip_V=128)
+        H, W, y = make_inputs(w, "cpu")
+        g = run_gpu(H, W, y, 128, "mean")
+        r = run_oracle(H, W, y, "mean")
+        if V == 1:
+            assert abs(g["loss"]) < 1e-6
+            assert np.abs(g["dH"]).max() < 1e-6 and np.abs(g["dW"]).max() < 1e-6
+            assert np.allclose(g["lse"], r["lse"], rtol=1e-3, atol=1e-3)
+        else:
+            assert_parity(g, r, dtype_name)
+
+
+def test_empty_batch(cuda_lib):
+    w = W2.with_sizes(N=0, d=64, V=300, strip_V=128)
+    H, W, y = make_inputs(w, "cpu")
+    for red in ("mean", "sum"):
+        g = run_gpu(H, W, y, 128, red)
+        assert g["n_valid"] == 0
+        assert np.isnan(g["loss"]) if red == "mean" else g["loss"] == 0.0
+        assert g["dH"].shape == (0, 64)
+        assert np.all(g["dW"] == 0)
+
+
+def test_all_rows_ignored(cuda_lib):
+    w = W2.with_sizes(N=200, d=64, V=700, strip_V=256)
+    H, W, y = make_inputs(w, "cpu")
+    y[:] = -100
+    g = run_gpu(H, W, y, 256, "mean")
+    r = run_oracle(H, W, y, "mean")
+    assert np.isnan(g["loss"]) and g["n_valid"] == 0
+    assert np.all(g["dH"] == 0) and np.all(g["dW"] == 0)
+    assert np.max(np.abs(g["lse"] - r["lse"]) / np.abs(r["lse"])) < 1e-3
+
+
+def test_custom_ignore_index(cuda_lib):
+    w = W3.with_sizes(N=300, d=96, V=900, strip_V=256)
+    H, W, y = make_inputs(w, "cpu")
+    y[y == -100] = 7  # the ignored rows now carry label 7, which is the ignore_index below
+    g = run_gpu(H, W, y, 256, "mean", ignore_index=7)
+    r = run_oracle(H, W, y, "mean", ignore_index=7)
+    assert_parity(g, r, "bf16")
+
+
+def test_bad_label_is_reported_and_row_excluded(cuda_lib):
+    w = W2.with_sizes(N=300, d=64, V=600, strip_V=256)
+    H, W, y = make_inputs(w, "cpu")
+    y[5] = 600      # == V
+    y[17] = -3      # negative, not ignore_index
+    with pytest.raises(LceError) as e:
+        run_gpu(H, W, y, 256, "mean")
+    assert e.value.name == "LCE_ERR_LABEL_OUT_OF_RANGE"
+    g = run_gpu(H, W, y, 256, "mean", check=False)
+    r = run_oracle(H, W, y, "mean")
+    assert r["n_valid"] == 298
+    assert_parity(g, r, "bf16")
+    assert np.all(g["dH"][[5, 17]] == 0)
+
+
+def test_bitwise_deterministic(cuda_lib):
+    w = W5.with_sizes(N=700, d=192, V=3000, strip_V=1024)
+    H, W, y = make_inputs(w, "cpu")
+    a = run_gpu(H, W, y, 1024, "sum")
+    b = run_gpu(H, W, y, 1024, "sum")
+    assert a["loss"] == b["loss"]
+    for k in ("lse", "dH", "dW"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_gradient_invariants_on_gpu_output(cuda_lib):
+    """sum_v dW_v = 0 (rows of softmax - onehot sum to 0) and <dW, W> = <dH, H> (both equal
+    sum_iv G_iv Z_iv), checked on the GPU outputs."""
+    w = W2.with_sizes(N=512, d=256, V=4000, strip_V=1024)
+    H, W, y = make_inputs(w, "cpu")
+    g = run_gpu(H, W, y, 1024, "mean")
+    colsum = np.abs(g["dW"].sum(axis=0)).max()
+    assert colsum <= 1e-2 * np.abs(g["dW"]).sum(axis=0).max()
+    Hn, Wn = H.double().numpy(), W.double().numpy()
+    a = float((g["dW"] * Wn).sum())
+    b = float((g["dH"] * Hn).sum())
+    assert abs(a - b) <= 1e-2 * max(abs(a), abs(b))
+
+
+def test_autograd_function_matches(cuda_lib):
+    w = W3.with_sizes(N=333, d=128, V=1500, strip_V=512)
+    H, W, y = make_inputs(w, "cpu")
+    Hd = H.cuda().requires_grad_(True)
+    Wd = W.cuda().requires_grad_(True)
+    loss = api.linear_cross_entropy(Hd, Wd, y.cuda(), strip_V=512)
+    loss.backward()
+    r = run_oracle(H, W, y, "mean")
+    assert abs(loss.item() - r["loss"]) <= 1e-3 * abs(r["loss"])
+    assert Hd.grad.dtype == torch.bfloat16 and Wd.grad.dtype == torch.bfloat16
+    assert rel_fro(Hd.grad.double().cpu().numpy(), r["dH"]) <= 1.5e-2
+    assert rel_fro(Wd.grad.double().cpu().numpy(), r["dW"]) <= 1.5e-2
+
+
+def test_workspace_bound_and_peak_memory(cuda_lib):
+    """The workspace grows with strip_V, not V, and the measured peak of a forward+backward is the
+    inputs + outputs + one workspace -- far below the N x V fp32 logits."""
+    N, d, V = 4096, 256, 65536
+    sizes = [api.lce_workspace_size(N, d, V, s) for s in (1024, 2048, 4096)]
+    assert sizes[0] < sizes[1] < sizes[2]
+    assert api.lce_workspace_size(N, d, 2 * V, 4096) == sizes[2]
+    w = W2.with_sizes(N=N, d=d, V=V, strip_V=2048)
+    H, W, y = make_inputs(w, "cuda")
+    torch.cuda.synchronize()
+    dH = torch.empty(N, d, device="cuda")
+    dW = torch.empty(V, d, device="cuda")
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    loss, lse, nv, ws = api.lce_forward(H, W, y, strip_V=2048)
+    api.lce_backward(H, W, y, lse, nv, torch.ones((), device="cuda"), strip_V=2048, workspace=ws,
+                     dH=dH, dW=dW)
+    torch.cuda.synchronize()
+    extra = torch.cuda.max_memory_allocated() - base
+    assert extra <= sizes[1] + 4 * N * 4 + 4096 + 2 * 1024 * 1024
+    assert extra < N * V * 4 / 10
