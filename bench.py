@@ -1,0 +1,396 @@
+"""Throughput of the fused linear cross-entropy forward+backward on GB300.
+
+One step = lce_forward + lce_backward over one batch (every strip of the vocabulary: logits and
+online log-sum-exp fold, strip combine, finalize; recomputed logits and gradient, dH and dW
+contractions), through the C ABI, on inputs already resident in HBM.  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--strip-V S]
+                  [--impl lce|reference] [--no-cpu-baseline]
+
+Under torchrun (N > 1) every rank runs its own batch of the same workload (weak scaling, no
+collective on the data path); rank 0 prints max-over-ranks timing.  ``--impl reference`` times
+the float64 CPU oracle on a bounded sample of the same workload (the reference arm).
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from memory_bounded_linear_gb300 import api, full_logits_bytes  # noqa: E402
+from memory_bounded_linear_gb300 import _lib  # noqa: E402
+from memory_bounded_linear_gb300.workloads import HEADLINE, WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s vs GB300 bf16 dense peak; peak MB"
+L2_BYTES = 129 * 1024 * 1024
+GEMM_KERNELS = ("tc_fwd_lse", "tc_bwd_grad", "tc_dh", "tc_dw",
+                "simt_fwd_lse", "simt_bwd_grad", "simt_dh", "simt_dw")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def strip_flops(w, strip_V):
+    """Algorithmic FLOPs of one launch of each GEMM kernel, per strip: 2 * N * d * strip width."""
+    out = []
+    for c0 in range(0, w.V, strip_V):
+        out.append(2 * w.N * w.d * min(strip_V, w.V - c0))
+    return out
+
+
+def cpu_baseline(w, H, W, y, target_s=15.0, min_tokens=16):
+    """Time the float64 oracle (as it stands) on a bounded token sample of the same workload:
+    one block of tokens through logits, lse, loss, dH rows and the block's dW contribution."""
+    import numpy as np
+
+    import oracle
+
+    Wn = W.cpu().to(torch.float64).numpy()
+    valid = (y != -100)
+    n_valid = int(valid.sum().item())
+    scale = (1.0 / max(n_valid, 1)) if w.reduction == "mean" else 1.0
+
+    def run(n):
+        Hb = H[:n].cpu().to(torch.float64).numpy()
+        yb = y[:n].cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.token_block_fwd_bwd(Hb, Wn, yb, scale)
+        return time.perf_counter() - t0
+
+    n = min_tokens
+    t = run(n)
+    if t < target_s / 4:
+        n = int(min(w.N, max(n, n * target_s / max(t, 1e-3) / 1.5)))
+        t = run(n)
+    cores = len(os.sched_getaffinity(0))
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", cores)))
+    del np
+    return {"value": n / t, "unit": "tokens/s", "cores": min(cores, threads), "kind": "oracle",
+            "seconds": t,
+            "sample": f"{n} tokens x full vocabulary ({w.V}) x d={w.d}, float64 numpy: "
+                      f"logits, lse, loss, dH rows and the block's dW contribution"}
+
+
+def run_reference(args, w):
+    """Reference arm: the float64 CPU oracle, timed on host cores, each step a bounded sample."""
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    H, W, y = make_inputs(w, "cpu", seed=0)
+    Wn = W.to(torch.float64).numpy()
+    n = args.ref_tokens
+    Hb = H[:n].to(torch.float64).numpy()
+    yb = y[:n].numpy()
+    n_valid = int((y != -100).sum().item())
+    scale = (1.0 / max(n_valid, 1)) if w.reduction == "mean" else 1.0
+    for _ in range(args.warmup):
+        oracle.token_block_fwd_bwd(Hb, Wn, yb, scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.token_block_fwd_bwd(Hb, Wn, yb, scale)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n / dt
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "N": w.N, "d": w.d, "V": w.V, "strip_V": args.strip_V,
+                   "reduction": w.reduction, "sample_tokens": n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} tokens of the workload per step, full vocabulary"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--strip-V", dest="strip_V", type=int, default=None)
+    ap.add_argument("--impl", default="lce", choices=["lce", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=64)
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    args.strip_V = args.strip_V or w.strip_V
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    lib = _lib.load()
+
+    N, d, V, S = w.N, w.d, w.V, args.strip_V
+    H, W, y = make_inputs(w, dev, seed=rank)
+    ws_bytes = api.lce_workspace_size(N, d, V, S, w.dtype)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    loss = torch.empty((), device=dev)
+    lse = torch.empty(N, device=dev)
+    nv = torch.empty((), dtype=torch.int64, device=dev)
+    dH = torch.empty(N, d, device=dev)
+    dW = torch.empty(V, d, device=dev)
+    one = torch.ones((), device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        api.lce_forward(H, W, y, strip_V=S, reduction=w.reduction, workspace=ws,
+                        out=(loss, lse, nv), stream=stream)
+        api.lce_backward(H, W, y, lse, nv, one, strip_V=S, reduction=w.reduction, workspace=ws,
+                         dH=dH, dW=dW, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # warm-up; peak memory of one forward+backward measured here
+    in_out_bytes = sum(t.numel() * t.element_size() for t in (H, W, y, lse, dH, dW))
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    api.lce_check_error(ws)
+    peak = torch.cuda.max_memory_allocated(dev)
+
+    # per-launch trace buffers (events recorded around every launch on the launching stream)
+    per_step = 2 * ((V + S - 1) // S) + 1 + 3 * ((V + S - 1) // S)
+    cap = per_step * args.steps + 16
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
+    for e in starts + stops:
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    arr = ctypes.c_void_p * cap
+    st_arr = arr(*[e.cuda_event for e in starts])
+    sp_arr = arr(*[e.cuda_event for e in stops])
+    ids = (ctypes.c_int32 * cap)()
+
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        barrier()
+        launches0 = lib.lce_launch_count()
+        _lib.check(lib.lce_trace_begin(st_arr, sp_arr, ids, cap), "lce_trace_begin")
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step()
+        t_stop.record(stream)
+        n_traced = lib.lce_trace_end()
+        launches = lib.lce_launch_count() - launches0
+        barrier()
+    ms_total = t_start.elapsed_time(t_stop)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = t.item()
+    ms = ms_total / args.steps
+    tokens_s = world * N / (ms / 1e3)
+    tflops = world * w.flops / (ms / 1e3) / 1e12
+    api.lce_check_error(ws)
+
+    # per-kernel device time from the trace (same timed region)
+    agg = {}
+    for i in range(n_traced):
+        name = lib.lce_kernel_name(ids[i]).decode()
+        a = agg.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += starts[i].elapsed_time(stops[i])
+    sflops = strip_flops(w, S)
+    gemm_flops_step = sum(sflops)
+    dominant = max((k for k in agg if k in GEMM_KERNELS), key=lambda k: agg[k][1])
+    n_launch, t_kernel = agg[dominant]
+    peaks, peak_src = measured_peaks()
+    peak_tf = peaks["bf16_tflops_sustained"] if w.dtype == "bf16" else None
+    achieved = gemm_flops_step * args.steps / (t_kernel / 1e3) / 1e12
+    roofline = {"kernel": dominant, "bound": "tensor" if w.dtype == "bf16" else "alu",
+                "achieved": achieved, "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": (achieved / peak_tf) if peak_tf else None,
+                "traffic": None, "launches": n_launch,
+                "avg_launch_ms": t_kernel / n_launch,
+                "peak_source": f"bf16_tflops_sustained ({peak_src})",
+                "per_kernel_ms_per_step": {k: v[1] / args.steps for k, v in sorted(agg.items())}}
+    clk = clocks.summary()
+
+    # end-to-end through the public API: pinned host inputs -> H2D -> fwd+bwd -> D2H of the loss
+    e2e = None
+    if not args.no_e2e:
+        Hh = H.cpu().pin_memory()
+        Wh = W.cpu().pin_memory()
+        yh = y.cpu().pin_memory()
+        loss_h = torch.empty((), dtype=torch.float32).pin_memory()
+        Hd, Wd, yd = torch.empty_like(H), torch.empty_like(W), torch.empty_like(y)
+
+        def e2e_step():
+            Hd.copy_(Hh, non_blocking=True)
+            Wd.copy_(Wh, non_blocking=True)
+            yd.copy_(yh, non_blocking=True)
+            api.lce_forward(Hd, Wd, yd, strip_V=S, reduction=w.reduction, workspace=ws,
+                            out=(loss, lse, nv), stream=stream)
+            api.lce_backward(Hd, Wd, yd, lse, nv, one, strip_V=S, reduction=w.reduction,
+                             workspace=ws, dH=dH, dW=dW, stream=stream)
+            loss_h.copy_(loss, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        k2 = max(3, args.steps // 2)
+        for _ in range(k2):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1) / k2
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = t.item()
+        e2e = {"value": world * N / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": (Hh.numel() * Hh.element_size() + Wh.numel() * Wh.element_size()
+                                      + yh.numel() * yh.element_size()),
+               "d2h_bytes_per_step": 4, "ms_per_step": e_ms}
+        del Hd, Wd, yd
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, H, W, y)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "N": N, "d": d, "V": V, "strip_V": S,
+                       "reduction": w.reduction, "parallelism": f"independent batch per GPU x{world}",
+                       "l2": "inputs larger than L2 (H+W = %.0f MB > 129 MB), no flush"
+                             % ((H.numel() * H.element_size() + W.numel() * W.element_size()) / 1e6)},
+            "tflops": tflops,
+            "frac_of_peak": tflops / peak_tf if peak_tf else None,
+            "peak_mb": peak / 1e6,
+            "peak_minus_inputs_outputs_mb": (peak - in_out_bytes) / 1e6,
+            "workspace_mb": ws_bytes / 1e6,
+            "full_logits_mb_avoided": full_logits_bytes(N, V) / 1e6,
+            "gpu_launches": launches,
+            "roofline": roofline,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -114,6 +114,12 @@ lce_status_t lce_check_error(const void* workspace, void* stream);
 const char* lce_status_string(lce_status_t status);
 
 /*
+ * Name of the CUDA error behind the most recent LCE_ERR_CUDA returned on the calling thread
+ * (e.g. "cudaErrorInvalidValue"), or "none".  Static storage; valid until the next call.
+ */
+const char* lce_last_cuda_error(void);
+
+/*
  * Number of kernels this library has launched in this process so far (all entry points, all
  * threads).  Used to count device launches inside a timed region.
  */

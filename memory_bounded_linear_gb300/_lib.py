@@ -33,6 +33,7 @@ _SIGNATURES = {
                                     ctypes.c_size_t, _c_p]),
     "lce_check_error": (ctypes.c_int, [_c_p, _c_p]),
     "lce_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "lce_last_cuda_error": (ctypes.c_char_p, []),
     "lce_launch_count": (ctypes.c_int64, []),
     "lce_trace_begin": (ctypes.c_int, [_c_p, _c_p, _c_p, ctypes.c_int32]),
     "lce_trace_end": (ctypes.c_int32, []),
@@ -74,4 +75,6 @@ def header_symbols() -> list[str]:
 
 def check(status: int, where: str) -> None:
     if status != LCE_OK:
+        if status == 5:
+            where = f"{where} ({load().lce_last_cuda_error().decode()})"
         raise LceError(status, where)

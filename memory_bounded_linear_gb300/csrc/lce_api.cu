@@ -61,7 +61,7 @@ signed char g_dev_ok[64];  // 0 unknown, 1 ok, -1 not sm_103
 
 lce_status_t check_device(int* num_sms) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LCE_ERR_CUDA;
+  if (note(cudaGetDevice(&dev)) != cudaSuccess) return LCE_ERR_CUDA;
   if (dev < 0 || dev >= 64) return LCE_ERR_UNSUPPORTED_DEVICE;
   if (g_dev_ok[dev] == 0) {
     int major = 0, minor = 0, sms = 0;
@@ -79,6 +79,12 @@ lce_status_t check_device(int* num_sms) {
 
 // --------------------------------------------------------------------------- launch bookkeeping
 std::atomic<int64_t> g_launches{0};
+thread_local const char* g_last_cuda_error = "none";
+
+cudaError_t note(cudaError_t e) {
+  if (e != cudaSuccess) g_last_cuda_error = cudaGetErrorName(e);
+  return e;
+}
 
 struct Trace {
   void* const* start = nullptr;
@@ -97,7 +103,10 @@ cudaError_t traced(int kid, cudaStream_t stream, F&& launch) {
     cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(g_trace.start[g_trace.n]), stream);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = launch();
+  // Drop a stale, non-sticky error another library may have left on this thread, so that the
+  // check after the launch reports only this launch (sticky errors are reported again anyway).
+  (void)cudaGetLastError();
+  cudaError_t e = note(launch());
   if (e != cudaSuccess) return e;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (rec) {
@@ -164,7 +173,7 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels, in
   float2* run = reinterpret_cast<float2*>(ws + L.off_run);
   float* tgt = reinterpret_cast<float*>(ws + L.off_tgt);
   float2* part = reinterpret_cast<float2*>(ws + L.off_part);
-  if (cudaMemsetAsync(ws, 0, WS_HEADER_BYTES, stream) != cudaSuccess) return LCE_ERR_CUDA;
+  if (note(cudaMemsetAsync(ws, 0, WS_HEADER_BYTES, stream)) != cudaSuccess) return LCE_ERR_CUDA;
 
   if (N > 0) {
     for (int64_t col0 = 0, s = 0; col0 < V; col0 += strip_V, ++s) {
@@ -212,7 +221,8 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, c
   void* G = ws + L.off_g;
   if (N == 0) {
     // no token: every logit-gradient row is absent, so dW = 0 (dH has no rows)
-    if (cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * d * sizeof(float), stream) != cudaSuccess)
+    if (note(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * d * sizeof(float), stream)) !=
+        cudaSuccess)
       return LCE_ERR_CUDA;
     return LCE_OK;
   }
@@ -246,10 +256,10 @@ lce_status_t lce_check_error(const void* workspace, void* stream_) {
   if (!workspace) return LCE_ERR_INVALID_ARG;
   unsigned flags = 0;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (cudaMemcpyAsync(&flags, workspace, sizeof(flags), cudaMemcpyDeviceToHost, stream) !=
+  if (note(cudaMemcpyAsync(&flags, workspace, sizeof(flags), cudaMemcpyDeviceToHost, stream)) !=
       cudaSuccess)
     return LCE_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return LCE_ERR_CUDA;
+  if (note(cudaStreamSynchronize(stream)) != cudaSuccess) return LCE_ERR_CUDA;
   if (flags & ERR_TIMEOUT) return LCE_ERR_TIMEOUT;
   if (flags & ERR_LABEL) return LCE_ERR_LABEL_OUT_OF_RANGE;
   return LCE_OK;
@@ -268,6 +278,8 @@ const char* lce_status_string(lce_status_t s) {
   }
   return "unknown status";
 }
+
+const char* lce_last_cuda_error(void) { return g_last_cuda_error; }
 
 int64_t lce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

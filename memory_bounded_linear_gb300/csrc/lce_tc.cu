@@ -499,7 +499,7 @@ cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) 
     default:
       return cudaErrorInvalidValue;
   }
-  if (!ok) return cudaErrorInvalidValue;
+  if (!ok) return cudaErrorInvalidResourceHandle;  // the tensor-map encoder refused the operand
   p.tiles_m = (p.M + BM - 1) / BM;
   p.tiles_n = (p.Ncols + BN - 1) / BN;
   p.num_tiles = p.tiles_m * p.tiles_n;
