@@ -56,6 +56,13 @@ bool make_layout(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t d
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // --------------------------------------------------------------------------- device checks
+thread_local const char* g_last_cuda_error = "none";
+
+cudaError_t note(cudaError_t e) {
+  if (e != cudaSuccess) g_last_cuda_error = cudaGetErrorName(e);
+  return e;
+}
+
 int g_sms[64];
 signed char g_dev_ok[64];  // 0 unknown, 1 ok, -1 not sm_103
 
@@ -79,12 +86,6 @@ lce_status_t check_device(int* num_sms) {
 
 // --------------------------------------------------------------------------- launch bookkeeping
 std::atomic<int64_t> g_launches{0};
-thread_local const char* g_last_cuda_error = "none";
-
-cudaError_t note(cudaError_t e) {
-  if (e != cudaSuccess) g_last_cuda_error = cudaGetErrorName(e);
-  return e;
-}
 
 struct Trace {
   void* const* start = nullptr;
