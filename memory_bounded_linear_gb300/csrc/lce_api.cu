@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <stdarg.h>
+#include <stdio.h>
+
 #include <algorithm>
 #include <atomic>
 
@@ -56,10 +59,14 @@ bool make_layout(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t d
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // --------------------------------------------------------------------------- device checks
-thread_local const char* g_last_cuda_error = "none";
+thread_local char g_last_error[384] = "none";
+thread_local bool g_detail_set = false;
 
+// Records the CUDA error of a failed call unless the failing step already described itself.
 cudaError_t note(cudaError_t e) {
-  if (e != cudaSuccess) g_last_cuda_error = cudaGetErrorName(e);
+  if (e != cudaSuccess && !g_detail_set)
+    snprintf(g_last_error, sizeof(g_last_error), "%s", cudaGetErrorName(e));
+  g_detail_set = false;
   return e;
 }
 
@@ -107,6 +114,7 @@ cudaError_t traced(int kid, cudaStream_t stream, F&& launch) {
   // Drop a stale, non-sticky error another library may have left on this thread, so that the
   // check after the launch reports only this launch (sticky errors are reported again anyway).
   (void)cudaGetLastError();
+  g_detail_set = false;
   cudaError_t e = note(launch());
   if (e != cudaSuccess) return e;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -143,6 +151,15 @@ lce_status_t common_checks(const void* H, const void* W, const int64_t* labels, 
 }
 
 }  // namespace
+
+void set_error_detail(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  g_detail_set = true;
+}
+
 }  // namespace lce
 
 using namespace lce;
@@ -280,7 +297,7 @@ const char* lce_status_string(lce_status_t s) {
   return "unknown status";
 }
 
-const char* lce_last_cuda_error(void) { return g_last_cuda_error; }
+const char* lce_last_cuda_error(void) { return g_last_error; }
 
 int64_t lce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -49,6 +49,10 @@ struct StripArgs {
   int first_strip;
 };
 
+// Records a human-readable description of the last failure on the calling thread (reported by
+// lce_last_cuda_error).  printf-style.
+void set_error_detail(const char* fmt, ...);
+
 // Tile widths of the two engines (columns of a logit tile).
 constexpr int TC_BN = 256;
 constexpr int SIMT_BN = 64;

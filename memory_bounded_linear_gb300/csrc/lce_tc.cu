@@ -441,16 +441,29 @@ EncodeTiledFn encode_fn() {
 // 2-D bf16 tensor map over a row-major [outer x inner] array with `ld` elements per row,
 // box = [box_outer x box_inner], 128-byte swizzle, zero fill outside the array.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
-              uint32_t box_inner, uint32_t box_outer) {
+              uint32_t box_inner, uint32_t box_outer, int mode, char operand) {
   EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
+  if (!enc) {
+    set_error_detail("cuTensorMapEncodeTiled entry point unavailable");
+    return false;
+  }
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {ld * 2};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUresult r =
+      enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error_detail("tensor map of operand %c, strip GEMM mode %d refused (CUresult %d; %llu x %llu"
+                     " elements, row stride %llu, box %u x %u, address %p)",
+                     operand, mode, static_cast<int>(r), static_cast<unsigned long long>(outer),
+                     static_cast<unsigned long long>(inner), static_cast<unsigned long long>(ld),
+                     box_outer, box_inner, ptr);
+    return false;
+  }
+  return true;
 }
 
 template <int MODE>
@@ -460,11 +473,19 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KParam
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(tc_strip_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      set_error_detail("shared-memory attribute of strip GEMM mode %d: %s", MODE,
+                       cudaGetErrorName(e));
+      return e;
+    }
     attr_set = true;
   }
   tc_strip_kernel<MODE><<<grid, THREADS, SMEM_BYTES, stream>>>(a, b, p);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    set_error_detail("launch of strip GEMM mode %d (grid %d, stream %p): %s", MODE, grid,
+                     static_cast<void*>(stream), cudaGetErrorName(e));
+  return e;
 }
 
 }  // namespace
@@ -480,21 +501,24 @@ cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) 
       p.Ncols = s.strip_cols;
       p.K = static_cast<int>(s.d);
       p.b_off = s.col0;
-      ok = make_map(&ma, s.H, s.d, s.N, s.d, BK, BM) && make_map(&mb, s.W, s.d, s.V, s.d, BK, BN);
+      ok = make_map(&ma, s.H, s.d, s.N, s.d, BK, BM, s.mode, 'A') &&
+           make_map(&mb, s.W, s.d, s.V, s.d, BK, BN, s.mode, 'B');
       break;
     case MODE_DH:
       p.M = static_cast<int>(s.N);
       p.Ncols = static_cast<int>(s.d);
       p.K = s.strip_cols;
       p.b_off = s.col0;
-      ok = make_map(&ma, s.G, s.ldg, s.N, s.ldg, BK, BM) && make_map(&mb, s.W, s.d, s.V, s.d, 64, BK);
+      ok = make_map(&ma, s.G, s.ldg, s.N, s.ldg, BK, BM, s.mode, 'A') &&
+           make_map(&mb, s.W, s.d, s.V, s.d, 64, BK, s.mode, 'B');
       break;
     case MODE_DW:
       p.M = s.strip_cols;
       p.Ncols = static_cast<int>(s.d);
       p.K = static_cast<int>(s.N);
       p.b_off = 0;
-      ok = make_map(&ma, s.G, s.ldg, s.N, s.ldg, 64, BK) && make_map(&mb, s.H, s.d, s.N, s.d, 64, BK);
+      ok = make_map(&ma, s.G, s.ldg, s.N, s.ldg, 64, BK, s.mode, 'A') &&
+           make_map(&mb, s.H, s.d, s.N, s.d, 64, BK, s.mode, 'B');
       break;
     default:
       return cudaErrorInvalidValue;
