@@ -205,8 +205,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override N (same d, V, strip and distributions; for small profiling runs)")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
+    if args.tokens:
+        w = w.with_sizes(N=args.tokens)
     args.strip_V = args.strip_V or w.strip_V
     if args.warmup < 3:
         args.warmup = 3
