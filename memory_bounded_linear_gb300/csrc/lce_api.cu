@@ -77,6 +77,10 @@ lce_status_t check_device(int* num_sms) {
   int dev = 0;
   if (note(cudaGetDevice(&dev)) != cudaSuccess) return LCE_ERR_CUDA;
   if (dev < 0 || dev >= 64) return LCE_ERR_UNSUPPORTED_DEVICE;
+  // Make the device's primary context current on this thread: the tensor maps are encoded with
+  // the driver API, which needs a current context, and a fresh thread (e.g. autograd's backward
+  // worker) has none until its first context-creating runtime call.
+  if (note(cudaSetDevice(dev)) != cudaSuccess) return LCE_ERR_CUDA;
   if (g_dev_ok[dev] == 0) {
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
