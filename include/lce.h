@@ -104,6 +104,39 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels,
                           void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Forward for callers that cannot allocate device memory.  The pages describe no such entry
+ * point: it is an addition of this library, with no counterpart in the papers.
+ *
+ * Some callers may not call cudaMalloc at all: a plugin of an engine that owns all device memory
+ * through its own pool and only lends out the buffers it planned; code enqueuing work while its
+ * stream is being captured into a CUDA graph; latency-critical code that cannot take the device
+ * synchronisation an allocation may bring.  This entry point computes exactly what lce_forward
+ * computes (same kernels, same results) but takes its workspace from a fixed array of
+ * LCE_STATIC_SCRATCH_BYTES (16 MiB) that the library keeps in device memory; it allocates nothing
+ * and frees nothing.  The caller still passes the inputs and the outputs (loss, lse, n_valid as
+ * in lce_forward).
+ *   - Size limit: when lce_workspace_size(N, d, V, strip_V, dtype) exceeds
+ *     LCE_STATIC_SCRATCH_BYTES the call returns LCE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing
+ *     (a smaller strip_V shrinks the workspace).
+ *   - device_error_flags (optional, device uint32, may be NULL) receives the device error bits
+ *     of this call once it has run: bit 0 = a label outside [0, V) that is not ignore_index,
+ *     bit 1 = a kernel wait timed out.  0 means no device-side error.
+ *   - Set-up: the first call on each device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture begins.
+ *   - Sharing: every GPU that loads the library holds the array until the process exits, and
+ *     every call on a device uses the same array, which keeps the last call's contents (the call
+ *     clears what must start at zero).  Calls whose work can overlap on the GPU -- on different
+ *     streams, or from several host threads -- race on the array; order them on one stream.
+ */
+#define LCE_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+lce_status_t lce_forward_static_scratch(const void* H, const void* W, const int64_t* labels,
+                                        int64_t N, int64_t d, int64_t V, int64_t ignore_index,
+                                        int64_t strip_V, lce_reduction_t reduction,
+                                        lce_dtype_t dtype, float* loss, float* lse,
+                                        int64_t* n_valid, uint32_t* device_error_flags,
+                                        void* stream);
+
+/*
  * Synchronises stream, then reads the workspace error flags written by the device:
  * LCE_ERR_TIMEOUT, else LCE_ERR_LABEL_OUT_OF_RANGE, else LCE_OK (LCE_ERR_CUDA if the copy or the
  * synchronisation itself fails).

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "liblce.so")
 
-SOURCES = ["lce_api.cu", "lce_tc.cu", "lce_simt.cu", "lce_reduce.cu"]
+SOURCES = ["lce_api.cu", "lce_tc.cu", "lce_simt.cu", "lce_reduce.cu", "lce_static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{INCLUDE}", f"-I{CSRC}"]
