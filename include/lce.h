@@ -7,9 +7,10 @@
  *     lse_i   = log sum_v exp(Z_iv)
  *     loss    = sum over valid rows of (lse_i - Z_{i,y_i}), divided by n_valid for MEAN
  *     dH      = G W,  dW = G^T H,  G = scale * (softmax(Z) - onehot(y)) on valid rows, 0 elsewhere
- *   "Long-Sequence MoE RL" blog, section "Linear CE: Avoiding Materialization of Full Logits":
- *   the linear output and the cross-entropy are organised so that the full logits are never
- *   generated or retained.  "Flattening Every Memory Peak in Long-Context MoE Training",
+ *   "Running 128K-Sequence MoE RL on 32 H100s" (blog), section "Linear CE: Avoiding
+ *   Materialization of Full Logits": the linear output and the cross-entropy are organised so
+ *   that the full logits are never generated or retained.
+ *   "Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training",
  *   section 3.2 and appendix C (Ring-DTP): each logit strip of the vocabulary is folded into a
  *   running per-token state and released, and backward recomputes each strip's gradient, so
  *   neither the full logits nor the full logit gradient is stored; section 2: the values and
@@ -66,8 +67,8 @@ typedef enum { LCE_BF16 = 0, LCE_F32 = 1 } lce_dtype_t;
  * Bytes of device workspace that lce_forward and lce_backward need for these sizes; 0 when the
  * arguments break a shape rule.  It grows as O(N * min(strip_V, V)) and never with V beyond the
  * strip: this is the closed-form per-call budget that can be checked before launch
- * ("Flattening Every Memory Peak", sections 3.5 and 6: the per-rank budget is fixed by the launch
- * configuration).  Layout: a 256-byte header (error flags) followed by the larger of the
+ * ("Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training", sections 3.5
+ * and 6: the per-rank budget is fixed by the launch configuration).  Layout: a 256-byte header (error flags) followed by the larger of the
  * forward region (running state, target logits, per-tile partial states of one strip) and the
  * backward region (one strip of the logit gradient, N x strip_V elements of the input dtype).
  */

@@ -3,8 +3,9 @@
 // combine:  folds the per-(tile, row) (max, sum-exp) partials of one vocabulary strip, in tile
 //           order, into the running per-token state (m, s):
 //             (m, s) (+) (m', s') = (M, s e^(m - M) + s' e^(m' - M)),  M = max(m, m')
-//           ("Flattening Every Memory Peak", section 3.2: each strip is folded into a running
-//           per-token state and released).  One thread per token, coalesced over tokens.
+//           ("Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training",
+//           section 3.2: each strip is folded into a running per-token state and released).
+//           One thread per token, coalesced over tokens.
 // finalize: lse_i = m_i + log s_i for every row; per-token loss lse_i - t_i on valid rows; the
 //           sum over rows in a fixed order in fp64 (one block, fixed per-thread strides and a
 //           fixed tree), n_valid, and the label-range check.

@@ -17,7 +17,7 @@
 // TMA zero-fills every box element outside the tensor, so ragged M, N and K edges contribute 0
 // to the products; the epilogues mask the columns beyond the strip / vocabulary.
 //
-// "Flattening Every Memory Peak in Long-Context MoE Training", section 3.2 / appendix C: each
+// "Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training", section 3.2 / appendix C: each
 // logit strip is folded into a running per-token state and released; backward recomputes the
 // strip and its gradient.  Here a strip's logits only ever live in TMEM.
 

@@ -6,10 +6,11 @@ shares no code with the CUDA library (no kernels, headers, helpers or tables).
 
 What it computes, and where the definition comes from
 -----------------------------------------------------
-"Long-Sequence MoE RL" blog (princepride.github.io), section "Linear CE: Avoiding
+"Running 128K-Sequence MoE RL on 32 H100s" (blog), section "Linear CE: Avoiding
 Materialization of Full Logits": the logits are the linear layer's output laid out along the
 vocabulary, followed by cross-entropy; Linear CE only avoids *holding* the N x V logits.
-"Flattening Every Memory Peak in Long-Context MoE Training" (paperlayer.ai), section 2: an
+"Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training",
+section 2: an
 operator of this kind must return the replaced (dense) implementation's forward values and
 gradients and change only the order of computation.  So the oracle is the plain dense
 definition, written out in float64:
@@ -29,7 +30,7 @@ Readings where the pages are silent (each is also listed in the design notes):
   * with mean reduction and no valid row, loss = 0/0 = NaN and dH = dW = 0 (G has no valid row);
   * lse is reported for every row, ignored or not (it does not depend on the label).
 
-``strip_forward`` follows the method's own order instead ("Flattening Every Memory Peak",
+``strip_forward`` follows the method's own order instead ("Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training",
 section 3.2 and appendix C, Ring-DTP): the vocabulary is cut into strips, each strip of
 logits is folded into a running per-token state and released.  The state is read as
 (running max m, running sum of exp(z - m), target logit t), an online log-sum-exp.
