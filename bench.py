@@ -46,6 +46,21 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value of x over all ranks (the slowest rank's time); x itself when alone."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def tokens_per_second(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own batch of tokens_per_rank per step."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -288,14 +303,9 @@ def main():
         n_traced = lib.lce_trace_end()
         launches = lib.lce_launch_count() - launches0
         barrier()
-    ms_total = t_start.elapsed_time(t_stop)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = t.item()
+    ms_total = max_over_ranks(t_start.elapsed_time(t_stop), world, dev)
     ms = ms_total / args.steps
-    tokens_s = world * N / (ms / 1e3)
+    tokens_s = tokens_per_second(world, N, ms)
     tflops = world * w.flops / (ms / 1e3) / 1e12
     api.lce_check_error(ws)
 
@@ -352,13 +362,8 @@ def main():
             e2e_step()
         e1.record(stream)
         barrier()
-        e_ms = e0.elapsed_time(e1) / k2
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = t.item()
-        e2e = {"value": world * N / (e_ms / 1e3), "unit": "tokens/s",
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / k2, world, dev)
+        e2e = {"value": tokens_per_second(world, N, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": (Hh.numel() * Hh.element_size() + Wh.numel() * Wh.element_size()
                                       + yh.numel() * yh.element_size()),
                "d2h_bytes_per_step": 4, "ms_per_step": e_ms}
