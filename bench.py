@@ -220,6 +220,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--tile-config", type=int, default=0, choices=[0, 1, 2],
+                    help="tensor-core tile variant: 0 automatic, 1 single-CTA, 2 CTA pairs")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override N (same d, V, strip and distributions; for small profiling runs)")
     args = ap.parse_args()
@@ -242,6 +244,7 @@ def main():
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     lib = _lib.load()
+    _lib.check(lib.lce_set_tile_config(args.tile_config), "lce_set_tile_config")
 
     N, d, V, S = w.N, w.d, w.V, args.strip_V
     H, W, y = make_inputs(w, dev, seed=rank)
@@ -381,6 +384,7 @@ def main():
             "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "N": N, "d": d, "V": V, "strip_V": S,
                        "reduction": w.reduction, "parallelism": f"independent batch per GPU x{world}",
+                       "tile_config": ["auto", "single-cta", "cta-pair"][args.tile_config],
                        "l2": "inputs larger than L2 (H+W = %.0f MB > 129 MB), no flush"
                              % ((H.numel() * H.element_size() + W.numel() * W.element_size()) / 1e6)},
             "tflops": tflops,

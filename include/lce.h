@@ -154,6 +154,16 @@ const char* lce_status_string(lce_status_t status);
 const char* lce_last_cuda_error(void);
 
 /*
+ * Tile variant of the bf16 tensor-core kernels, process-wide (not thread-safe; for tests and
+ * tuning).  0 = automatic (default): CTA pairs whenever the GEMM has more than 128 rows,
+ * 1 = single-CTA 128x256 tiles (tcgen05 cta_group::1, 4-stage pipeline),
+ * 2 = CTA-pair 256x256 tiles (cta_group::2 on a cluster of 2, 6-stage pipeline).
+ * Results are equal within rounding across variants; each variant is deterministic.
+ * LCE_ERR_INVALID_ARG for any other value.
+ */
+lce_status_t lce_set_tile_config(int32_t config);
+
+/*
  * Number of kernels this library has launched in this process so far (all entry points, all
  * threads).  Used to count device launches inside a timed region.
  */

@@ -303,6 +303,12 @@ const char* lce_status_string(lce_status_t s) {
 
 const char* lce_last_cuda_error(void) { return g_last_error; }
 
+lce_status_t lce_set_tile_config(int32_t config) {
+  if (config < 0 || config > 2) return LCE_ERR_INVALID_ARG;
+  g_tile_config = config;
+  return LCE_OK;
+}
+
 int64_t lce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 lce_status_t lce_trace_begin(void* const* start_events, void* const* stop_events,

@@ -33,25 +33,36 @@
 namespace lce {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = TC_BN;  // 256
-constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;        // 16 KB
-constexpr int B_BYTES = BN * BK * 2;        // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BM = 128;     // accumulator rows held by one CTA (TMEM lanes)
+constexpr int BN = TC_BN;  // 256 columns per tile
+constexpr int BK = 64;     // one 128-byte swizzle span of bf16
 constexpr int MN_BOX_BYTES = 64 * BK * 2;   // one 64(MN) x 64(K) box of an MN-major operand
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int MAX_STAGES = 6;
 constexpr int CTL_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + CTL_BYTES;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // a wait longer than 2 s is treated as a hang
-constexpr int RASTER_GROUP = 16;                   // row tiles per rasterisation group
+
+// Tile geometry.  Single: one CTA computes a 128 x 256 tile and holds all of B.  Pair: the two
+// CTAs of a cluster compute a 256 x 256 tile with cta_group::2 MMAs; each holds its 128 rows of
+// A and half (128 columns) of B, so a stage is 32 KB and six stages fit.
+template <bool PAIR>
+struct Cfg {
+  static constexpr int TILE_M = PAIR ? 2 * BM : BM;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // tile columns whose B rows this CTA loads
+  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + CTL_BYTES;
+  static constexpr int RASTER_GROUP = PAIR ? 8 : 16;  // row tiles per rasterisation group
+  static_assert(STAGES <= MAX_STAGES, "control block sized for MAX_STAGES");
+};
 
 struct Ctl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -109,14 +120,15 @@ __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity, ui
     if (ptx::globaltimer() - t0 > limit_ns) return;
 }
 
-// Grouped rasterisation: RASTER_GROUP row tiles sweep the column tiles together, so the tiles
+// Grouped rasterisation: `group` row tiles sweep the column tiles together, so the tiles
 // resident at one time share a few A row-blocks and B column-blocks through L2.
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& tm, int& tn) {
-  const int per_group = RASTER_GROUP * tiles_n;
-  const int group = tile / per_group;
-  const int first_m = group * RASTER_GROUP;
-  const int gm = min(tiles_m - first_m, RASTER_GROUP);
-  const int r = tile - group * per_group;
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group, int& tm,
+                                            int& tn) {
+  const int per_group = group * tiles_n;
+  const int g = tile / per_group;
+  const int first_m = g * group;
+  const int gm = min(tiles_m - first_m, group);
+  const int r = tile - g * per_group;
   tm = first_m + r % gm;
   tn = r / gm;
 }
@@ -133,13 +145,16 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_base, int k16) {
   return ptx::sw128_desc(tile_base + k16 * 16 * 128, MN_BOX_BYTES, 1024);
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_strip_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const KParams p) {
+  using Cf = Cfg<PAIR>;
+  constexpr int STAGES = Cf::STAGES;
+  constexpr int STAGE_BYTES = Cf::STAGE_BYTES;
   constexpr bool A_MN = (MODE == MODE_DW);
   constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
-  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(Cf::TILE_M, BN, A_MN, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -150,6 +165,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0 = the pair's MMA issuer
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -158,18 +176,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_addr(&ctl->tfull[b]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->tempty[b]), 4);  // one arrival per epilogue warp
+      // one arrival per epilogue warp (of both CTAs of a pair)
+      ptx::mbar_init(ptx::smem_addr(&ctl->tempty[b]), PAIR ? 8 : 4);
     }
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
     ctl->abort_flag = 0;
     ptx::fence_barrier_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), TMEM_COLS);
-    ptx::tmem_relinquish();
+    if (PAIR) {
+      ptx::tmem_alloc_pair(ptx::smem_addr(&ctl->tmem_base), TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
     ptx::tc_fence_before();
   }
-  __syncthreads();
+  // Barriers initialised and TMEM allocated in both CTAs before either uses the other's.
+  if (PAIR) ptx::cluster_sync(); else __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
@@ -181,30 +206,37 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       int stage = 0;
       uint32_t ph = 0;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = unit; ok && tile < p.num_tiles; tile += units) {
         int tm, tn;
-        tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+        tile_coords(tile, p.tiles_m, p.tiles_n, Cf::RASTER_GROUP, tm, tn);
+        const int m0 = tm * Cf::TILE_M + static_cast<int>(rank) * BM;       // first A row here
+        const int n0 = tn * BN + static_cast<int>(rank) * Cf::B_ROWS * PAIR;  // first B row here
         for (int kb = 0; kb < p.nkb; ++kb) {
           const uint32_t empty = ptx::smem_addr(&ctl->empty[stage]);
-          const uint32_t full = ptx::smem_addr(&ctl->full[stage]);
+          const uint32_t full_local = ptx::smem_addr(&ctl->full[stage]);
           if (!wait_bar(empty, ph ^ 1u, abort_flag, p.err)) { ok = false; break; }
           const uint32_t sa = base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+          const uint32_t sb = sa + Cf::A_BYTES;
+          // In a pair every stage's bytes (of both CTAs) are counted on the issuer's barrier.
+          const uint32_t full = PAIR ? ptx::mapa_shared(full_local, 0) : full_local;
+          if (rank == 0) ptx::mbar_arrive_expect_tx(full_local, (PAIR ? 2 : 1) * STAGE_BYTES);
+          auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
+            if (PAIR) ptx::tma_load_2d_pair(dst, m, x, y, full);
+            else ptx::tma_load_2d(dst, m, x, y, full);
+          };
           if (A_MN) {
 #pragma unroll
-            for (int c = 0; c < BM / 64; ++c)
-              ptx::tma_load_2d(sa + c * MN_BOX_BYTES, &tmA, tm * BM + c * 64, kb * BK, full);
+            for (int c = 0; c < BM / 64; ++c) load(sa + c * MN_BOX_BYTES, &tmA, m0 + c * 64, kb * BK);
           } else {
-            ptx::tma_load_2d(sa, &tmA, kb * BK, tm * BM, full);
+            load(sa, &tmA, kb * BK, m0);
           }
           if (B_MN) {
             const int krow = (MODE == MODE_DH ? p.b_off : 0) + kb * BK;
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              ptx::tma_load_2d(sb + c * MN_BOX_BYTES, &tmB, tn * BN + c * 64, krow, full);
+            for (int c = 0; c < Cf::B_ROWS / 64; ++c)
+              load(sb + c * MN_BOX_BYTES, &tmB, n0 + c * 64, krow);
           } else {
-            ptx::tma_load_2d(sb, &tmB, kb * BK, p.b_off + tn * BN, full);
+            load(sb, &tmB, kb * BK, p.b_off + n0);
           }
           if (++stage == STAGES) { stage = 0; ph ^= 1u; }
         }
@@ -217,13 +249,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       bool ok = true;
       int stage = 0;
       uint32_t ph = 0;
       int acc = 0;
       uint32_t aph = 0;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = unit; ok && tile < p.num_tiles; tile += units) {
         if (!wait_bar(ptx::smem_addr(&ctl->tempty[acc]), aph ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
@@ -237,24 +269,30 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           ptx::tc_fence_after();
           const uint32_t sa = base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sb = sa + Cf::A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = A_MN ? desc_mnmajor(sa, k) : desc_kmajor(sa, k);
             const uint64_t bd = B_MN ? desc_mnmajor(sb, k) : desc_kmajor(sb, k);
-            ptx::tc_mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+            if (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+            else ptx::tc_mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
           }
-          ptx::tc_commit(ptx::smem_addr(&ctl->empty[stage]));  // frees the stage when read
+          // frees the stage (in both CTAs of a pair) once the MMAs have read it
+          if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&ctl->empty[stage]), 0x3);
+          else ptx::tc_commit(ptx::smem_addr(&ctl->empty[stage]));
           if (++stage == STAGES) { stage = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        ptx::tc_commit(ptx::smem_addr(&ctl->tfull[acc]));  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue warps (of both CTAs of a pair)
+        if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&ctl->tfull[acc]), 0x3);
+        else ptx::tc_commit(ptx::smem_addr(&ctl->tfull[acc]));
         acc ^= 1;
         if (acc == 0) aph ^= 1u;
       }
       if (!ok) {
         // Make sure no MMA is still writing TMEM before it is released.
-        ptx::tc_commit(ptx::smem_addr(&ctl->drain));
+        if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&ctl->drain), 0x1);
+        else ptx::tc_commit(ptx::smem_addr(&ctl->drain));
         wait_bar_drain(ptx::smem_addr(&ctl->drain), 0, 100000000ull);
       }
     }
@@ -269,15 +307,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     int acc = 0;
     uint32_t aph = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    for (int tile = unit; tile < p.num_tiles; tile += units) {
       int tm, tn;
-      tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+      tile_coords(tile, p.tiles_m, p.tiles_n, Cf::RASTER_GROUP, tm, tn);
       const uint32_t tfull = ptx::smem_addr(&ctl->tfull[acc]);
-      const uint32_t tempty = ptx::smem_addr(&ctl->tempty[acc]);
+      const uint32_t tempty_local = ptx::smem_addr(&ctl->tempty[acc]);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const int row = tm * Cf::TILE_M + static_cast<int>(rank) * BM + r_in;
+      // hand the accumulator back to the MMA issuer (in the pair's first CTA)
+      auto release = [&]() {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_local, 0));
+          else ptx::mbar_arrive(tempty_local);
+        }
+      };
 
       if (MODE == MODE_FWD_LSE || MODE == MODE_BWD_G) {
-        const int row = tm * BM + r_in;
         const bool row_ok = row < p.M;
         const int tcol0 = tn * BN;
         const int ncols = min(BN, p.strip_cols - tcol0);  // valid columns of this tile (>= 1)
@@ -318,9 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             s = s * exp2f(fmaf(m, LOG2E, nml)) + cs;
             m = mn;
           }
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(tempty);
+          release();
           if (row_ok) {
             p.part[static_cast<size_t>(tn) * p.M + row] = make_float2(m, s);
             if (tloc >= 0) p.tgt[row] = t;
@@ -363,13 +408,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                                     packed[4 * i + 3]);
             }
           }
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(tempty);
+          release();
         }
       } else {
         // MODE_DH / MODE_DW: C (+)= accumulator, fp32
-        const int row = tm * BM + r_in;
         const bool row_ok = row < p.c_rows;
         float* crow = p.C + static_cast<size_t>(row) * p.ldc;
         if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
@@ -402,19 +444,20 @@ __global__ void __launch_bounds__(THREADS, 1)
               if (col + j < p.c_cols) crow[col + j] = (p.accumulate ? crow[col + j] : 0.f) + v[j];
           }
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(tempty);
+        release();
       }
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
   }
 
-  __syncthreads();
+  // Every role of both CTAs is done (and no remote arrival is still on its way) before TMEM is
+  // released and the CTAs exit.
+  if (PAIR) ptx::cluster_sync(); else __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else ptx::tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -466,13 +509,15 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return true;
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KParams& p, int grid,
                         cudaStream_t stream) {
+  using Cf = Cfg<PAIR>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_strip_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(tc_strip_kernel<MODE, PAIR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cf::SMEM_BYTES);
     if (e != cudaSuccess) {
       set_error_detail("shared-memory attribute of strip GEMM mode %d: %s", MODE,
                        cudaGetErrorName(e));
@@ -480,17 +525,32 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KParam
     }
     attr_set = true;
   }
-  tc_strip_kernel<MODE><<<grid, THREADS, SMEM_BYTES, stream>>>(a, b, p);
-  const cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_strip_kernel<MODE, PAIR>, a, b, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess)
-    set_error_detail("launch of strip GEMM mode %d (grid %d, stream %p): %s", MODE, grid,
-                     static_cast<void*>(stream), cudaGetErrorName(e));
+    set_error_detail("launch of strip GEMM mode %d%s (grid %d, stream %p): %s", MODE,
+                     PAIR ? " (CTA pairs)" : "", grid, static_cast<void*>(stream),
+                     cudaGetErrorName(e));
   return e;
 }
 
-}  // namespace
-
-cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) {
+template <bool PAIR>
+cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
+  using Cf = Cfg<PAIR>;
   KParams p{};
   CUtensorMap ma, mb;
   bool ok = true;
@@ -502,7 +562,7 @@ cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) 
       p.K = static_cast<int>(s.d);
       p.b_off = s.col0;
       ok = make_map(&ma, s.H, s.d, s.N, s.d, BK, BM, s.mode, 'A') &&
-           make_map(&mb, s.W, s.d, s.V, s.d, BK, BN, s.mode, 'B');
+           make_map(&mb, s.W, s.d, s.V, s.d, BK, Cf::B_ROWS, s.mode, 'B');
       break;
     case MODE_DH:
       p.M = static_cast<int>(s.N);
@@ -524,7 +584,7 @@ cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) 
       return cudaErrorInvalidValue;
   }
   if (!ok) return cudaErrorInvalidResourceHandle;  // the tensor-map encoder refused the operand
-  p.tiles_m = (p.M + BM - 1) / BM;
+  p.tiles_m = (p.M + Cf::TILE_M - 1) / Cf::TILE_M;
   p.tiles_n = (p.Ncols + BN - 1) / BN;
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.nkb = (p.K + BK - 1) / BK;
@@ -549,13 +609,29 @@ cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) 
   p.c_cols = s.c_cols;
   p.err = s.err;
   p.first_strip = s.first_strip;
-  const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+  // persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than there are tiles
+  const int units = PAIR ? num_sms / 2 : num_sms;
+  const int grid = (p.num_tiles < units ? p.num_tiles : units) * (PAIR ? 2 : 1);
   switch (s.mode) {
-    case MODE_FWD_LSE: return launch_mode<MODE_FWD_LSE>(ma, mb, p, grid, stream);
-    case MODE_BWD_G: return launch_mode<MODE_BWD_G>(ma, mb, p, grid, stream);
-    case MODE_DH: return launch_mode<MODE_DH>(ma, mb, p, grid, stream);
-    default: return launch_mode<MODE_DW>(ma, mb, p, grid, stream);
+    case MODE_FWD_LSE: return launch_mode<MODE_FWD_LSE, PAIR>(ma, mb, p, grid, stream);
+    case MODE_BWD_G: return launch_mode<MODE_BWD_G, PAIR>(ma, mb, p, grid, stream);
+    case MODE_DH: return launch_mode<MODE_DH, PAIR>(ma, mb, p, grid, stream);
+    default: return launch_mode<MODE_DW, PAIR>(ma, mb, p, grid, stream);
   }
+}
+
+}  // namespace
+
+int g_tile_config = 0;
+
+cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) {
+  // Rows of C: tokens for the logit, gradient and dH GEMMs, strip columns for dW.
+  const int64_t rows = (s.mode == MODE_DW) ? s.strip_cols : s.N;
+  bool pair;
+  if (g_tile_config == 1) pair = false;
+  else if (g_tile_config == 2) pair = true;
+  else pair = rows > BM;  // pairs need a second 128-row half to be worth launching
+  return pair ? run<true>(s, stream, num_sms) : run<false>(s, stream, num_sms);
 }
 
 }  // namespace lce

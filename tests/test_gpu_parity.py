@@ -36,6 +36,43 @@ def test_bf16_reduced_workloads(cuda_lib, w):
     parity_case(w)
 
 
+@pytest.fixture
+def tile_config(cuda_lib):
+    """Force one tile variant of the tensor-core kernels for a test, then restore automatic."""
+    def set_(cfg):
+        assert cuda_lib.lce_set_tile_config(cfg) == 0
+    yield set_
+    cuda_lib.lce_set_tile_config(0)
+
+
+@pytest.mark.parametrize("cfg", [1, 2], ids=["single-cta", "cta-pair"])
+@pytest.mark.parametrize("w", [
+    W2.with_sizes(N=300, d=136, V=1000, strip_V=384),
+    W3.with_sizes(N=517, d=256, V=2048, strip_V=512),
+    W5.with_sizes(N=640, d=320, V=2500, strip_V=1024),
+    W2.with_sizes(N=129, d=64, V=257, strip_V=128),
+    W2.with_sizes(N=40, d=64, V=700, strip_V=384),
+], ids=["ragged", "ignore10", "outliers-sum", "tile+1", "N<128"])
+def test_bf16_each_tile_variant(cuda_lib, tile_config, cfg, w):
+    """Both tile variants (single-CTA 128x256 and CTA-pair 256x256) match the oracle on ragged
+    shapes, including GEMMs with fewer rows than one tile of the variant."""
+    tile_config(cfg)
+    parity_case(w)
+
+
+def test_tile_variants_agree(cuda_lib, tile_config):
+    w = W4.with_sizes(N=700, d=192, V=3000, strip_V=1024)
+    H, W, y = make_inputs(w, "cpu")
+    out = {}
+    for cfg in (1, 2):
+        tile_config(cfg)
+        out[cfg] = run_gpu(H, W, y, 1024, "mean")
+    assert abs(out[1]["loss"] - out[2]["loss"]) <= 1e-5 * abs(out[1]["loss"])
+    assert np.max(np.abs(out[1]["lse"] - out[2]["lse"])) <= 1e-4
+    assert rel_fro(out[2]["dH"], out[1]["dH"]) <= 1e-3
+    assert rel_fro(out[2]["dW"], out[1]["dW"]) <= 1e-3
+
+
 @pytest.mark.parametrize("w", [
     WT.with_sizes(N=100, d=72, V=1000, strip_V=384),
     WT.with_sizes(N=70, d=8, V=130, strip_V=128, reduction="sum"),
