@@ -197,12 +197,21 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels, in
   float2* part = reinterpret_cast<float2*>(ws + L.off_part);
   if (note(cudaMemsetAsync(ws, 0, WS_HEADER_BYTES, stream)) != cudaSuccess) return LCE_ERR_CUDA;
 
+  // The forward keeps one (max, sum-exp) partial per token and logit tile of the columns a launch
+  // covers.  When the partials of the whole vocabulary fit in the workspace sized for strip_V (the
+  // backward's gradient strip is larger whenever strip_V >= V/64), one persistent launch covers
+  // every strip; otherwise there is one launch per strip.  Either way the workspace is the same.
+  const int64_t tiles_all = (V + L.bn - 1) / L.bn;
+  const bool one_launch =
+      L.off_part + static_cast<size_t>(tiles_all) * static_cast<size_t>(N) * sizeof(float2) <=
+      L.total;
+  const int64_t fwd_step = one_launch ? V : strip_V;
   if (N > 0) {
-    for (int64_t col0 = 0, s = 0; col0 < V; col0 += strip_V, ++s) {
+    for (int64_t col0 = 0, s = 0; col0 < V; col0 += fwd_step, ++s) {
       StripArgs a{};
       a.mode = MODE_FWD_LSE;
       a.col0 = static_cast<int>(col0);
-      a.strip_cols = static_cast<int>(std::min(strip_V, V - col0));
+      a.strip_cols = static_cast<int>(std::min(fwd_step, V - col0));
       a.H = H; a.W = W; a.d = d; a.N = N; a.V = V;
       a.part = part; a.tgt = tgt;
       a.labels = labels; a.ignore_index = ignore_index;

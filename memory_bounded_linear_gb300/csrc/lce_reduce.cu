@@ -5,7 +5,7 @@
 //             (m, s) (+) (m', s') = (M, s e^(m - M) + s' e^(m' - M)),  M = max(m, m')
 //           ("Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training",
 //           section 3.2: each strip is folded into a running per-token state and released).
-//           One thread per token, coalesced over tokens.
+//           Eight warps share the tiles of 32 tokens; coalesced over tokens.
 // finalize: lse_i = m_i + log s_i for every row; per-token loss lse_i - t_i on valid rows; the
 //           sum over rows in a fixed order in fp64 (one block, fixed per-thread strides and a
 //           fixed tree), n_valid, and the label-range check.
@@ -24,13 +24,29 @@ __device__ __forceinline__ float2 fold(float2 a, float2 b) {
   return make_float2(M, a.y * expf(a.x - M) + b.y * expf(b.x - M));
 }
 
-__global__ void combine_kernel(const float2* __restrict__ part, int tiles, int64_t N,
-                               float2* __restrict__ run, int first) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= N) return;
-  float2 st = first ? make_float2(-INFINITY, 0.f) : run[i];
-  for (int t = 0; t < tiles; ++t) st = fold(st, part[static_cast<size_t>(t) * N + i]);
-  run[i] = st;
+// One block folds 32 consecutive tokens: warp w takes tiles w, w + 8, w + 16, ... of its lane's
+// token (coalesced over the 32 tokens), then lane j of warp 0 folds the eight warp states in warp
+// order and the result into the running state -- a fixed order, so the result is deterministic.
+constexpr int COMBINE_WARPS = 8;
+
+__global__ void __launch_bounds__(COMBINE_WARPS * 32)
+    combine_kernel(const float2* __restrict__ part, int tiles, int64_t N, float2* __restrict__ run,
+                   int first) {
+  __shared__ float2 st_w[COMBINE_WARPS][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  float2 st = make_float2(-INFINITY, 0.f);
+  if (i < N)
+    for (int t = warp; t < tiles; t += COMBINE_WARPS)
+      st = fold(st, part[static_cast<size_t>(t) * N + i]);
+  st_w[warp][lane] = st;
+  __syncthreads();
+  if (warp == 0 && i < N) {
+    float2 acc = first ? make_float2(-INFINITY, 0.f) : run[i];
+#pragma unroll
+    for (int w = 0; w < COMBINE_WARPS; ++w) acc = fold(acc, st_w[w][lane]);
+    run[i] = acc;
+  }
 }
 
 constexpr int FIN_THREADS = 1024;
@@ -88,9 +104,9 @@ __global__ void __launch_bounds__(FIN_THREADS)
 cudaError_t launch_combine(const float2* part, int tiles, int64_t N, float2* run, int first,
                            cudaStream_t stream) {
   if (N == 0) return cudaSuccess;
-  const int threads = 256;
-  const int64_t blocks = (N + threads - 1) / threads;
-  combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(part, tiles, N, run, first);
+  const int64_t blocks = (N + 31) / 32;
+  combine_kernel<<<static_cast<unsigned>(blocks), COMBINE_WARPS * 32, 0, stream>>>(part, tiles, N,
+                                                                                 run, first);
   return cudaGetLastError();
 }
 
