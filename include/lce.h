@@ -96,6 +96,8 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels,
  * MEAN, dloss for SUM) into one strip of workspace, then accumulates dH += G_s W_s and writes
  * dW_s = G_s^T H on the tensor cores.  Writes dH (device fp32 [N x d], overwritten) and dW
  * (device fp32 [V x d], overwritten).  dW rows are each written exactly once (deterministic).
+ * The workspace need not come from lce_forward; its header (error flags) is cleared first, so
+ * lce_check_error afterwards reports the problems this call found.
  */
 lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels,
                           const float* lse, const int64_t* n_valid, const float* dloss,

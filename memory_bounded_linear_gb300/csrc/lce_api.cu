@@ -250,6 +250,8 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, c
   char* ws = static_cast<char*>(workspace);
   unsigned* err = reinterpret_cast<unsigned*>(ws);
   void* G = ws + L.off_g;
+  // error flags and scheduler counters start from zero (the workspace may be fresh memory)
+  if (note(cudaMemsetAsync(ws, 0, WS_HEADER_BYTES, stream)) != cudaSuccess) return LCE_ERR_CUDA;
   if (N == 0) {
     // no token: every logit-gradient row is absent, so dW = 0 (dH has no rows)
     if (note(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * d * sizeof(float), stream)) !=

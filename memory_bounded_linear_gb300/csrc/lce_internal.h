@@ -10,7 +10,11 @@ namespace lce {
 constexpr unsigned ERR_LABEL = 1u;     // a label outside [0, V) that is not ignore_index
 constexpr unsigned ERR_TIMEOUT = 2u;   // a kernel-side wait ran out of time
 
+// Workspace header: word 0 error flags; words 16-17 the tile scheduler's ticket counters (zero
+// between launches: cleared with the header by each entry point, reset by every launch's last
+// CTA).  Both entry points clear the header before their first launch.
 constexpr size_t WS_HEADER_BYTES = 256;
+constexpr int WS_SCHED_WORD = 16;
 
 // The four epilogues of the strip GEMM engine.
 enum Mode : int {

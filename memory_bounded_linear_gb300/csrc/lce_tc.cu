@@ -44,6 +44,12 @@ constexpr int CTL_BYTES = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // a wait longer than 2 s is treated as a hang
 
+// Pair tiles per rasterisation group (build-time tunable): more tiles per group re-read the
+// column operand less often but keep a larger row panel live in L2.
+#ifndef LCE_PAIR_RASTER_GROUP
+#define LCE_PAIR_RASTER_GROUP 8
+#endif
+
 // Tile geometry.  Single: one CTA computes a 128 x 256 tile and holds all of B.  Pair: the two
 // CTAs of a cluster compute a 256 x 256 tile with cta_group::2 MMAs; each holds its 128 rows of
 // A and half (128 columns) of B, so a stage is 32 KB and six stages fit.
@@ -56,9 +62,12 @@ struct Cfg {
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + CTL_BYTES;
-  static constexpr int RASTER_GROUP = PAIR ? 8 : 16;  // row tiles per rasterisation group
+  static constexpr int RASTER_GROUP = PAIR ? LCE_PAIR_RASTER_GROUP : 16;  // row tiles per group
   static_assert(STAGES <= MAX_STAGES, "control block sized for MAX_STAGES");
 };
+
+// Tiles handed out by the dynamic scheduler wait in a small ring until every role has read them.
+constexpr int TQ = 4;
 
 struct Ctl {
   uint64_t full[MAX_STAGES];
@@ -66,6 +75,9 @@ struct Ctl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t tq_full[TQ];
+  uint64_t tq_empty[TQ];
+  int tq[TQ];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -91,20 +103,26 @@ struct KParams {
   int64_t ldc;
   int accumulate, c_rows, c_cols;
   unsigned* err;
+  unsigned* sched;  // [0] next tile ticket, [1] units finished; both zero between launches
   int first_strip;
 };
 
 // Bounded wait on an mbarrier phase.  Gives up after WAIT_LIMIT_NS (or at once when another role
 // already gave up), raising the CTA's abort flag and the workspace timeout bit.
+template <bool CLUSTER_ACQUIRE = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned* err) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  auto try_once = [&]() {
+    return CLUSTER_ACQUIRE ? ptx::mbar_try_wait_cluster(bar, parity)
+                           : ptx::mbar_try_wait(bar, parity);
+  };
+  if (try_once()) return true;
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
     if (*abort_flag) return false;
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if (try_once()) return true;
     if (ptx::globaltimer() - t0 > WAIT_LIMIT_NS) {
       *abort_flag = 1;
       atomicOr(err, ERR_TIMEOUT);
@@ -132,6 +150,62 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
   tm = first_m + r % gm;
   tn = r / gm;
 }
+
+// Dynamic tile scheduler.  The producer thread of the (first) CTA takes tickets from a global
+// counter -- tiles come out in raster order, so the tiles in flight at any moment stay together in
+// the raster however unevenly the SMs progress, and operands keep being shared through L2 -- and
+// posts each tile id into the ring `tq` of both CTAs of a pair.  Every other role reads the ids
+// from its own CTA's ring and hands the slot back.  -1 ends the sequence.
+template <bool PAIR>
+struct TileQueue {
+  Ctl* ctl;
+  volatile int* abort_flag;
+  unsigned* err;
+  int slot;
+  uint32_t ph;
+
+  __device__ __forceinline__ void advance() {
+    if (++slot == TQ) { slot = 0; ph ^= 1u; }
+  }
+
+  // Scheduler: the next ticket, posted to both CTAs.  Returns -1 at the end (and after a
+  // timeout); the last unit to finish clears the counters for the next launch.
+  __device__ __forceinline__ int post(unsigned* sched, int num_tiles, int units) {
+    const uint32_t empty = ptx::smem_addr(&ctl->tq_empty[slot]);
+    if (!wait_bar<PAIR>(empty, ph ^ 1u, abort_flag, err)) return -1;
+    int t = static_cast<int>(atomicAdd(&sched[0], 1u));
+    if (t >= num_tiles) t = -1;
+    ctl->tq[slot] = t;
+    const uint32_t full = ptx::smem_addr(&ctl->tq_full[slot]);
+    if (PAIR) {
+      ptx::st_shared_cluster(ptx::mapa_shared(ptx::smem_addr(&ctl->tq[slot]), 1), t);
+      ptx::mbar_arrive_cluster(ptx::mapa_shared(full, 1));
+    }
+    ptx::mbar_arrive(full);
+    advance();
+    if (t < 0 && atomicAdd(&sched[1], 1u) == static_cast<unsigned>(units - 1)) {
+      atomicExch(&sched[0], 0u);
+      atomicExch(&sched[1], 0u);
+    }
+    return t;
+  }
+
+  // Reader: the next tile id of this CTA's ring.  `mask` names the lanes of the calling warp that
+  // read it together; the slot is handed back (once per warp) after all of them have.
+  __device__ __forceinline__ int take(unsigned mask) {
+    const uint32_t full = ptx::smem_addr(&ctl->tq_full[slot]);
+    int t = -1;
+    if (wait_bar<PAIR>(full, ph, abort_flag, err)) t = ctl->tq[slot];
+    __syncwarp(mask);
+    if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(mask) - 1)) {
+      const uint32_t empty = ptx::smem_addr(&ctl->tq_empty[slot]);
+      if (PAIR) ptx::mbar_arrive_cluster(ptx::mapa_shared(empty, 0));
+      else ptx::mbar_arrive(empty);
+    }
+    advance();
+    return t;
+  }
+};
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_base, int k16) {
   // K-major, 128B swizzle: rows of 128 bytes, 8-row swizzle atoms 1024 bytes apart; the k-th
@@ -166,7 +240,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0 = the pair's MMA issuer
-  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
@@ -180,6 +253,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mbar_init(ptx::smem_addr(&ctl->tempty[b]), PAIR ? 8 : 4);
     }
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
+    for (int i = 0; i < TQ; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->tq_full[i]), 1);
+      // readers: MMA issuer + 4 epilogue warps, plus the second CTA's producer and 4 epilogue warps
+      ptx::mbar_init(ptx::smem_addr(&ctl->tq_empty[i]), PAIR ? 10 : 5);
+    }
     ctl->abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -206,7 +284,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       int stage = 0;
       uint32_t ph = 0;
-      for (int tile = unit; ok && tile < p.num_tiles; tile += units) {
+      TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u};
+      while (ok) {
+        const int tile = (rank == 0) ? tq.post(p.sched, p.num_tiles, units) : tq.take(1u);
+        if (tile < 0) break;
         int tm, tn;
         tile_coords(tile, p.tiles_m, p.tiles_n, Cf::RASTER_GROUP, tm, tn);
         const int m0 = tm * Cf::TILE_M + static_cast<int>(rank) * BM;       // first A row here
@@ -255,7 +336,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t ph = 0;
       int acc = 0;
       uint32_t aph = 0;
-      for (int tile = unit; ok && tile < p.num_tiles; tile += units) {
+      TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u};
+      while (ok) {
+        if (tq.take(1u) < 0) break;
         if (!wait_bar(ptx::smem_addr(&ctl->tempty[acc]), aph ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
@@ -307,7 +390,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     int acc = 0;
     uint32_t aph = 0;
-    for (int tile = unit; tile < p.num_tiles; tile += units) {
+    TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u};
+    while (true) {
+      const int tile = tq.take(0xffffffffu);
+      if (tile < 0) break;
       int tm, tn;
       tile_coords(tile, p.tiles_m, p.tiles_n, Cf::RASTER_GROUP, tm, tn);
       const uint32_t tfull = ptx::smem_addr(&ctl->tfull[acc]);
@@ -609,6 +695,7 @@ cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
   p.c_cols = s.c_cols;
   p.err = s.err;
   p.first_strip = s.first_strip;
+  p.sched = s.err + WS_SCHED_WORD;
   // persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than there are tiles
   const int units = PAIR ? num_sms / 2 : num_sms;
   const int grid = (p.num_tiles < units ? p.num_tiles : units) * (PAIR ? 2 : 1);
