@@ -61,6 +61,33 @@ def tokens_per_second(world: int, tokens_per_rank: int, ms_per_step: float) -> f
     return world * tokens_per_rank / (ms_per_step / 1e3)
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each tensor-core
+# kernel, from one ncu capture of this benchmark's timed step at full size (one pass per
+# kernel), keyed by workload, strip width and kernel.  They describe the kernel source whose
+# SHA-256 is KERNEL_SOURCE_SHA256; once the source differs they no longer apply (traffic: null).
+KERNEL_SOURCES = ("memory_bounded_linear_gb300/csrc/lce_tc.cu",
+                  "memory_bounded_linear_gb300/csrc/ptx.cuh",
+                  "memory_bounded_linear_gb300/csrc/lce_internal.h")
+KERNEL_SOURCE_SHA256 = None
+MEASURED_TRAFFIC = {}
+
+
+def kernel_source_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, strip_V: int, kernel: str):
+    """Bytes per launch measured for this kernel source, else None."""
+    if KERNEL_SOURCE_SHA256 is None or kernel_source_sha256() != KERNEL_SOURCE_SHA256:
+        return None
+    return MEASURED_TRAFFIC.get((workload, strip_V, kernel))
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -329,7 +356,7 @@ def main():
     roofline = {"kernel": dominant, "bound": "tensor" if w.dtype == "bf16" else "alu",
                 "achieved": achieved, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": (achieved / peak_tf) if peak_tf else None,
-                "traffic": None, "launches": n_launch,
+                "traffic": measured_traffic(w.name, S, dominant), "launches": n_launch,
                 "avg_launch_ms": t_kernel / n_launch,
                 "peak_source": f"bf16_tflops_sustained ({peak_src})",
                 "per_kernel_ms_per_step": {k: v[1] / args.steps for k, v in sorted(agg.items())}}
