@@ -68,8 +68,15 @@ def tokens_per_second(world: int, tokens_per_rank: int, ms_per_step: float) -> f
 KERNEL_SOURCES = ("memory_bounded_linear_gb300/csrc/lce_tc.cu",
                   "memory_bounded_linear_gb300/csrc/ptx.cuh",
                   "memory_bounded_linear_gb300/csrc/lce_internal.h")
-KERNEL_SOURCE_SHA256 = None
-MEASURED_TRAFFIC = {}
+KERNEL_SOURCE_SHA256 = "40a989f21f060b01fcc5a45b2e813eab872b2f56884a6431b4c7e74198720653"
+MEASURED_TRAFFIC = {
+    # N=32768 d=6144 V=151552, strip 16384: the timed step's 31 launches (1 forward over the whole
+    # vocabulary, 10 strips x 3 backward kernels), averaged over each kernel's launches
+    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse"): 30426832640,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd_grad"): 4407631846,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_dh"): 9309541964,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_dw"): 11470691584,
+}
 
 
 def kernel_source_sha256() -> str:

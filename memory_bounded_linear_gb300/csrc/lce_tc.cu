@@ -41,6 +41,10 @@ constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int MAX_STAGES = 6;
 constexpr int CTL_BYTES = 256;
+// Epilogue output staging: per epilogue warp two 4 KB buffers, each a 32-row x 128-byte box
+// (32 fp32 or 64 bf16 columns) in the 128-byte-swizzled layout a TMA store reads.
+constexpr int STAGE_BUF_BYTES = 32 * 128;
+constexpr int STAGING_BYTES = 4 * 2 * STAGE_BUF_BYTES;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // a wait longer than 2 s is treated as a hang
 
@@ -61,7 +65,7 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + CTL_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + CTL_BYTES;
   static constexpr int RASTER_GROUP = PAIR ? LCE_PAIR_RASTER_GROUP : 16;  // row tiles per group
   static_assert(STAGES <= MAX_STAGES, "control block sized for MAX_STAGES");
 };
@@ -222,7 +226,7 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_base, int k16) {
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_strip_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const KParams p) {
+                    const __grid_constant__ CUtensorMap tmC, const KParams p) {
   using Cf = Cfg<PAIR>;
   constexpr int STAGES = Cf::STAGES;
   constexpr int STAGE_BYTES = Cf::STAGE_BYTES;
@@ -234,7 +238,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;  // 128B-swizzled tiles need 1024B alignment
   uint8_t* smem = smem_raw + (base - raw_addr);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  const uint32_t staging = base + STAGES * STAGE_BYTES;  // 1024-aligned (stage sizes are)
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES + STAGING_BYTES);
   volatile int* abort_flag = &ctl->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -462,11 +467,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             atomicOr(p.err, ERR_LABEL);
           const float scale = label_ok ? scale_valid : 0.f;
           const float nl = label_ok ? -p.lse[row] * LOG2E : 0.f;
-          __nv_bfloat16* grow = p.G + static_cast<size_t>(row) * p.ldg + tcol0;
+          // The warp's 32 rows go out as 32 x 64-column boxes through two staging buffers.
+          const uint32_t wbuf0 = staging + q * 2 * STAGE_BUF_BYTES;
+          const int box_row = tm * Cf::TILE_M + static_cast<int>(rank) * BM + q * 32;
           if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
           ptx::tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
+            const uint32_t sbuf = wbuf0 + ((c >> 1) & 1) * STAGE_BUF_BYTES;
+            if ((c & 1) == 0 && c >= 4) {  // the buffer's previous box must have been read
+              if (lane == 0) ptx::bulk_wait_read<1>();
+              __syncwarp();
+            }
             uint32_t packed[16];
             if (c * 32 < ncols) {
               float v[32];
@@ -486,20 +498,35 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 16; ++j) packed[j] = 0u;
             }
-            if (row_ok) {
-              uint4* dst = reinterpret_cast<uint4*>(grow + c * 32);
+            // this thread's row of the box: 128 bytes, 16-byte chunk jj at (jj ^ (row % 8)) -- the
+            // 128-byte swizzle the store's tensor map expects (also spreads the warp over banks)
+            const uint32_t rowaddr = sbuf + lane * 128;
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                    packed[4 * i + 3]);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t jj = (c & 1) * 4 + kk;
+              ptx::st_shared_v4(rowaddr + ((jj ^ (lane & 7)) << 4), packed[4 * kk],
+                                packed[4 * kk + 1], packed[4 * kk + 2], packed[4 * kk + 3]);
+            }
+            if (c & 1) {
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                ptx::tma_store_2d(&tmC, sbuf, tcol0 + (c - 1) * 32, box_row);
+                ptx::bulk_commit();
+              }
             }
           }
           release();
+          if (lane == 0) ptx::bulk_wait_read<0>();  // both buffers free for the next tile
+          __syncwarp();
         }
       } else {
         // MODE_DH / MODE_DW: C (+)= accumulator, fp32
-        const bool row_ok = row < p.c_rows;
-        float* crow = p.C + static_cast<size_t>(row) * p.ldc;
+        // The warp's 32 rows go out as 32 x 32 fp32 boxes through two staging buffers; the tensor
+        // map clips rows and columns outside C.  Accumulation into dH is a TMA add (one add per
+        // element per launch, in strip order: deterministic).
+        const uint32_t wbuf0 = staging + q * 2 * STAGE_BUF_BYTES;
+        const int box_row = tm * Cf::TILE_M + static_cast<int>(rank) * BM + q * 32;
         if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
         ptx::tc_fence_after();
 #pragma unroll 1
@@ -508,33 +535,34 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (col >= p.c_cols) break;  // same for every thread of the CTA
           float v[32];
           ptx::tmem_load32(tbase + c * 32, v);
-          if (!row_ok) continue;
-          if (col + 32 <= p.c_cols) {
-            float4* dst = reinterpret_cast<float4*>(crow + col);
-            if (p.accumulate) {
-              float4 o[8];
+          const uint32_t sbuf = wbuf0 + (c & 1) * STAGE_BUF_BYTES;
+          if (c >= 2) {  // the buffer's previous box must have been read
+            if (lane == 0) ptx::bulk_wait_read<1>();
+            __syncwarp();
+          }
+          const uint32_t rowaddr = sbuf + lane * 128;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) o[i] = dst[i];
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(o[i].x + v[4 * i], o[i].y + v[4 * i + 1],
-                                     o[i].z + v[4 * i + 2], o[i].w + v[4 * i + 3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col + j < p.c_cols) crow[col + j] = (p.accumulate ? crow[col + j] : 0.f) + v[j];
+          for (int jj = 0; jj < 8; ++jj)
+            ptx::st_shared_v4(rowaddr + ((static_cast<uint32_t>(jj) ^ (lane & 7)) << 4),
+                              __float_as_uint(v[4 * jj]), __float_as_uint(v[4 * jj + 1]),
+                              __float_as_uint(v[4 * jj + 2]), __float_as_uint(v[4 * jj + 3]));
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (p.accumulate) ptx::tma_reduce_add_2d(&tmC, sbuf, col, box_row);
+            else ptx::tma_store_2d(&tmC, sbuf, col, box_row);
+            ptx::bulk_commit();
           }
         }
         release();
+        if (lane == 0) ptx::bulk_wait_read<0>();  // both buffers free for the next tile
+        __syncwarp();
       }
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
+    if (lane == 0) ptx::bulk_wait<0>();  // this warp's output stores have landed
+    __syncwarp();
   }
 
   // Every role of both CTAs is done (and no remote arrival is still on its way) before TMEM is
@@ -570,18 +598,19 @@ EncodeTiledFn encode_fn() {
 // 2-D bf16 tensor map over a row-major [outer x inner] array with `ld` elements per row,
 // box = [box_outer x box_inner], 128-byte swizzle, zero fill outside the array.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
-              uint32_t box_inner, uint32_t box_outer, int mode, char operand) {
+              uint32_t box_inner, uint32_t box_outer, int mode, char operand, bool fp32 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     set_error_detail("cuTensorMapEncodeTiled entry point unavailable");
     return false;
   }
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint64_t strides[1] = {ld * (fp32 ? 4 : 2)};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r =
-      enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+      enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+          const_cast<void*>(ptr), dims, strides, box, estr,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -596,8 +625,8 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 }
 
 template <int MODE, bool PAIR>
-cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KParams& p, int grid,
-                        cudaStream_t stream) {
+cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const KParams& p, int grid, cudaStream_t stream) {
   using Cf = Cfg<PAIR>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -625,7 +654,7 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const KParam
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_strip_kernel<MODE, PAIR>, a, b, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_strip_kernel<MODE, PAIR>, a, b, c, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess)
     set_error_detail("launch of strip GEMM mode %d%s (grid %d, stream %p): %s", MODE,
@@ -638,7 +667,7 @@ template <bool PAIR>
 cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
   using Cf = Cfg<PAIR>;
   KParams p{};
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc;  // operands A and B; mc: where the epilogue's TMA stores go
   bool ok = true;
   switch (s.mode) {
     case MODE_FWD_LSE:
@@ -649,6 +678,9 @@ cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
       p.b_off = s.col0;
       ok = make_map(&ma, s.H, s.d, s.N, s.d, BK, BM, s.mode, 'A') &&
            make_map(&mb, s.W, s.d, s.V, s.d, BK, Cf::B_ROWS, s.mode, 'B');
+      // gradient strip [N x ldg] bf16, written as 64-column x 32-row boxes
+      if (ok) ok = (s.mode == MODE_BWD_G) ? make_map(&mc, s.G, s.ldg, s.N, s.ldg, 64, 32, s.mode, 'G')
+                                         : (mc = ma, true);
       break;
     case MODE_DH:
       p.M = static_cast<int>(s.N);
@@ -656,7 +688,8 @@ cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
       p.K = s.strip_cols;
       p.b_off = s.col0;
       ok = make_map(&ma, s.G, s.ldg, s.N, s.ldg, BK, BM, s.mode, 'A') &&
-           make_map(&mb, s.W, s.d, s.V, s.d, 64, BK, s.mode, 'B');
+           make_map(&mb, s.W, s.d, s.V, s.d, 64, BK, s.mode, 'B') &&
+           make_map(&mc, s.C, s.d, s.N, s.ldc, 32, 32, s.mode, 'C', true);  // dH [N x d] fp32
       break;
     case MODE_DW:
       p.M = s.strip_cols;
@@ -664,7 +697,8 @@ cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
       p.K = static_cast<int>(s.N);
       p.b_off = 0;
       ok = make_map(&ma, s.G, s.ldg, s.N, s.ldg, 64, BK, s.mode, 'A') &&
-           make_map(&mb, s.H, s.d, s.N, s.d, 64, BK, s.mode, 'B');
+           make_map(&mb, s.H, s.d, s.N, s.d, 64, BK, s.mode, 'B') &&
+           make_map(&mc, s.C, s.d, s.strip_cols, s.ldc, 32, 32, s.mode, 'C', true);  // dW_s
       break;
     default:
       return cudaErrorInvalidValue;
@@ -700,10 +734,10 @@ cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
   const int units = PAIR ? num_sms / 2 : num_sms;
   const int grid = (p.num_tiles < units ? p.num_tiles : units) * (PAIR ? 2 : 1);
   switch (s.mode) {
-    case MODE_FWD_LSE: return launch_mode<MODE_FWD_LSE, PAIR>(ma, mb, p, grid, stream);
-    case MODE_BWD_G: return launch_mode<MODE_BWD_G, PAIR>(ma, mb, p, grid, stream);
-    case MODE_DH: return launch_mode<MODE_DH, PAIR>(ma, mb, p, grid, stream);
-    default: return launch_mode<MODE_DW, PAIR>(ma, mb, p, grid, stream);
+    case MODE_FWD_LSE: return launch_mode<MODE_FWD_LSE, PAIR>(ma, mb, mc, p, grid, stream);
+    case MODE_BWD_G: return launch_mode<MODE_BWD_G, PAIR>(ma, mb, mc, p, grid, stream);
+    case MODE_DH: return launch_mode<MODE_DH, PAIR>(ma, mb, mc, p, grid, stream);
+    default: return launch_mode<MODE_DW, PAIR>(ma, mb, mc, p, grid, stream);
   }
 }
 
