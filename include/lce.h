@@ -166,6 +166,17 @@ const char* lce_last_cuda_error(void);
 lce_status_t lce_set_tile_config(int32_t config);
 
 /*
+ * Test hook for the timeout path (process-wide, not thread-safe).  With on = 1 the next bf16
+ * tensor-core launch withholds the first k-block of operands it would load: nothing arrives on
+ * that stage's barrier, so the MMA issuer's bounded wait runs out after its 2 s limit.  Every role
+ * of every CTA then gives up, lets copies in flight land, frees its tensor memory and returns;
+ * the launch sets the workspace timeout bit, so lce_check_error reports LCE_ERR_TIMEOUT, and the
+ * CUDA context stays usable.  The hook clears itself after that one launch.  No fault, trap or
+ * endless loop is involved.  LCE_ERR_INVALID_ARG unless on is 0 or 1.
+ */
+lce_status_t lce_test_inject_stall(int32_t on);
+
+/*
  * Number of kernels this library has launched in this process so far (all entry points, all
  * threads).  Used to count device launches inside a timed region.
  */

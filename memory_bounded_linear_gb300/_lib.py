@@ -38,6 +38,7 @@ _SIGNATURES = {
     "lce_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "lce_last_cuda_error": (ctypes.c_char_p, []),
     "lce_set_tile_config": (ctypes.c_int, [ctypes.c_int32]),
+    "lce_test_inject_stall": (ctypes.c_int, [ctypes.c_int32]),
     "lce_launch_count": (ctypes.c_int64, []),
     "lce_trace_begin": (ctypes.c_int, [_c_p, _c_p, _c_p, ctypes.c_int32]),
     "lce_trace_end": (ctypes.c_int32, []),

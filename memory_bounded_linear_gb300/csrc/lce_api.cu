@@ -320,6 +320,12 @@ lce_status_t lce_set_tile_config(int32_t config) {
   return LCE_OK;
 }
 
+lce_status_t lce_test_inject_stall(int32_t on) {
+  if (on != 0 && on != 1) return LCE_ERR_INVALID_ARG;
+  g_inject_stall = on;
+  return LCE_OK;
+}
+
 int64_t lce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 lce_status_t lce_trace_begin(void* const* start_events, void* const* stop_events,

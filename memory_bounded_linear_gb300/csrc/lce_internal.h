@@ -64,6 +64,8 @@ constexpr int SIMT_BN = 64;
 // Tile variant of the tensor-core engine: 0 automatic, 1 single-CTA 128x256 tiles, 2 CTA-pair
 // 256x256 tiles (set through lce_set_tile_config).
 extern int g_tile_config;
+// Test hook: when set, the next tensor-core launch withholds its first k-block (then it clears).
+extern int g_inject_stall;
 
 // Tensor-core (tcgen05) engine, bf16 operands: lce_tc.cu
 cudaError_t tc_strip_gemm(const StripArgs& a, cudaStream_t stream, int num_sms);

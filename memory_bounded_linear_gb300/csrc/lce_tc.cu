@@ -109,6 +109,7 @@ struct KParams {
   unsigned* err;
   unsigned* sched;  // [0] next tile ticket, [1] units finished; both zero between launches
   int first_strip;
+  int inject_stall;  // test hook (lce_test_inject_stall): withhold the first k-block
 };
 
 // Bounded wait on an mbarrier phase.  Gives up after WAIT_LIMIT_NS (or at once when another role
@@ -303,6 +304,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!wait_bar(empty, ph ^ 1u, abort_flag, p.err)) { ok = false; break; }
           const uint32_t sa = base + stage * STAGE_BYTES;
           const uint32_t sb = sa + Cf::A_BYTES;
+          if (p.inject_stall && kb == 0 && stage == 0 && ph == 0) {
+            // Test hook: withhold the very first k-block (no bytes, no arrival), so the MMA
+            // issuer's wait on it runs out and the launch takes its timeout path.
+            if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+            continue;
+          }
           // In a pair every stage's bytes (of both CTAs) are counted on the issuer's barrier.
           const uint32_t full = PAIR ? ptx::mapa_shared(full_local, 0) : full_local;
           if (rank == 0) ptx::mbar_arrive_expect_tx(full_local, (PAIR ? 2 : 1) * STAGE_BYTES);
@@ -730,6 +737,8 @@ cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
   p.err = s.err;
   p.first_strip = s.first_strip;
   p.sched = s.err + WS_SCHED_WORD;
+  p.inject_stall = g_inject_stall;  // one launch only
+  g_inject_stall = 0;
   // persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than there are tiles
   const int units = PAIR ? num_sms / 2 : num_sms;
   const int grid = (p.num_tiles < units ? p.num_tiles : units) * (PAIR ? 2 : 1);
@@ -744,6 +753,7 @@ cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
 }  // namespace
 
 int g_tile_config = 0;
+int g_inject_stall = 0;
 
 cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) {
   // Rows of C: tokens for the logit, gradient and dH GEMMs, strip columns for dW.
