@@ -68,9 +68,12 @@ typedef enum { LCE_BF16 = 0, LCE_F32 = 1 } lce_dtype_t;
  * arguments break a shape rule.  It grows as O(N * min(strip_V, V)) and never with V beyond the
  * strip: this is the closed-form per-call budget that can be checked before launch
  * ("Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training", sections 3.5
- * and 6: the per-rank budget is fixed by the launch configuration).  Layout: a 256-byte header (error flags) followed by the larger of the
- * forward region (running state, target logits, per-tile partial states of one strip) and the
- * backward region (one strip of the logit gradient, N x strip_V elements of the input dtype).
+ * and 6: the per-rank budget is fixed by the launch configuration).  Layout: a 256-byte header
+ * (error flags) followed by the larger of the forward region (running state, target logits,
+ * per-tile partial states of one strip) and the backward region: one strip of the logit gradient
+ * (N x strip_V elements of the input dtype), or two for bf16 when the backward of a strip is small
+ * (ceil(N/256) * ceil(d/256) <= 512): each backward launch then overlaps dH and dW of one strip
+ * with the gradient of the next.
  */
 size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dtype);
 

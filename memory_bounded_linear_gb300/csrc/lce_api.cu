@@ -17,6 +17,9 @@ namespace lce {
 namespace {
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+// Largest dH job (in 256 x 256 tiles) whose backward step is overlapped with the next strip's
+// gradient computation (a few waves of the GPU's 76 CTA pairs).
+constexpr int64_t kOverlapMaxTiles = 512;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -26,6 +29,8 @@ struct Layout {
   int64_t ldg;      // row stride of the strip gradient workspace (elements)
   int tiles;        // logit tiles per full strip
   size_t off_run, off_tgt, off_part, off_g;
+  size_t g_bytes;   // one gradient strip
+  bool overlap_bwd; // two gradient strips: each backward launch also computes the next gradient
   size_t total;
 };
 
@@ -51,7 +56,13 @@ bool make_layout(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t d
   L->off_part = L->off_tgt + align256(n * sizeof(float));
   const size_t fwd_end = L->off_part + align256(static_cast<size_t>(L->tiles) * n * sizeof(float2));
   L->off_g = WS_HEADER_BYTES;
-  const size_t bwd_end = L->off_g + align256(n * static_cast<size_t>(L->ldg) * elt);
+  L->g_bytes = align256(n * static_cast<size_t>(L->ldg) * elt);
+  // A small backward step (dH of one strip: few 256 x 256 tiles, a launch of a few waves) runs
+  // overlapped with the next strip's gradient in one launch, which needs a second gradient strip;
+  // a large one fills the GPU by itself and keeps the single strip.
+  const int64_t dh_tiles = ((N + 255) / 256) * ((d + 255) / 256);
+  L->overlap_bwd = (dt == LCE_BF16) && dh_tiles <= kOverlapMaxTiles;
+  const size_t bwd_end = L->off_g + (L->overlap_bwd ? 2 : 1) * L->g_bytes;
   L->total = std::max(fwd_end, bwd_end);
   return true;
 }
@@ -132,10 +143,8 @@ cudaError_t traced(int kid, cudaStream_t stream, F&& launch) {
 }
 
 cudaError_t strip_gemm(const StripArgs& a, lce_dtype_t dt, cudaStream_t stream, int num_sms) {
-  if (dt == LCE_BF16) {
-    static const int kid[4] = {K_TC_FWD, K_TC_BWD_G, K_TC_DH, K_TC_DW};
-    return traced(kid[a.mode], stream, [&] { return tc_strip_gemm(a, stream, num_sms); });
-  }
+  if (dt == LCE_BF16)  // the bf16 backward goes through tc_strip_jobs, never through here
+    return traced(K_TC_FWD, stream, [&] { return tc_strip_gemm(a, stream, num_sms); });
   static const int kid[4] = {K_SIMT_FWD, K_SIMT_BWD_G, K_SIMT_DH, K_SIMT_DW};
   return traced(kid[a.mode], stream, [&] { return simt_strip_gemm(a, stream); });
 }
@@ -259,16 +268,57 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, c
       return LCE_ERR_CUDA;
     return LCE_OK;
   }
-  for (int64_t col0 = 0, s = 0; col0 < V; col0 += strip_V, ++s) {
+  auto strip_job = [&](int64_t s, int mode, void* g) {
     StripArgs a{};
+    const int64_t col0 = s * strip_V;
+    a.mode = mode;
     a.col0 = static_cast<int>(col0);
     a.strip_cols = static_cast<int>(std::min(strip_V, V - col0));
     a.H = H; a.W = W; a.d = d; a.N = N; a.V = V;
-    a.G = G; a.ldg = L.ldg;
+    a.G = g; a.ldg = L.ldg;
     a.labels = labels; a.ignore_index = ignore_index;
     a.lse = lse; a.dloss = dloss; a.n_valid = n_valid; a.reduction = reduction;
     a.err = err; a.first_strip = (s == 0);
-
+    a.ldc = d; a.c_cols = static_cast<int>(d);
+    if (mode == MODE_DH) {
+      a.C = dH; a.accumulate = (s > 0); a.c_rows = static_cast<int>(N);
+    } else if (mode == MODE_DW) {
+      a.C = dW + static_cast<size_t>(col0) * d; a.c_rows = a.strip_cols;
+    }
+    return a;
+  };
+  const int64_t S = (V + strip_V - 1) / strip_V;
+  if (dtype == LCE_BF16) {
+    auto run = [&](StripArgs* jobs, int nj) {
+      return traced(K_TC_BWD, stream, [&] { return tc_strip_jobs(jobs, nj, stream, num_sms); });
+    };
+    if (L.overlap_bwd) {
+      // Step s computes dH and dW of strip s-1 (from gradient buffer (s-1) % 2, the longer
+      // reductions first) together with the gradient strip s (into buffer s % 2): one persistent
+      // launch per step, S + 1 steps.  dH accumulates strip after strip in order.
+      void* gbuf[2] = {G, static_cast<char*>(G) + L.g_bytes};
+      for (int64_t s = 0; s <= S; ++s) {
+        StripArgs jobs[3];
+        int nj = 0;
+        if (s >= 1) {
+          jobs[nj++] = strip_job(s - 1, MODE_DH, gbuf[(s - 1) & 1]);
+          jobs[nj++] = strip_job(s - 1, MODE_DW, gbuf[(s - 1) & 1]);
+        }
+        if (s < S) jobs[nj++] = strip_job(s, MODE_BWD_G, gbuf[s & 1]);
+        if (run(jobs, nj) != cudaSuccess) return LCE_ERR_CUDA;
+      }
+    } else {
+      // Per strip: its gradient, then dH and dW from it -- three launches, one gradient strip.
+      for (int64_t s = 0; s < S; ++s)
+        for (int mode : {MODE_BWD_G, MODE_DH, MODE_DW}) {
+          StripArgs job = strip_job(s, mode, G);
+          if (run(&job, 1) != cudaSuccess) return LCE_ERR_CUDA;
+        }
+    }
+    return LCE_OK;
+  }
+  for (int64_t col0 = 0, s = 0; col0 < V; col0 += strip_V, ++s) {
+    StripArgs a = strip_job(s, MODE_BWD_G, G);
     a.mode = MODE_BWD_G;
     if (strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;
 
@@ -347,9 +397,8 @@ int32_t lce_trace_end(void) {
 }
 
 const char* lce_kernel_name(int32_t id) {
-  static const char* names[K_NUM] = {"tc_fwd_lse", "tc_bwd_grad", "tc_dh", "tc_dw",
-                                     "simt_fwd_lse", "simt_bwd_grad", "simt_dh", "simt_dw",
-                                     "combine", "finalize"};
+  static const char* names[K_NUM] = {"tc_fwd_lse", "tc_bwd", "simt_fwd_lse", "simt_bwd_grad",
+                                     "simt_dh", "simt_dw", "combine", "finalize"};
   return (id >= 0 && id < K_NUM) ? names[id] : nullptr;
 }
 

@@ -25,10 +25,11 @@ enum Mode : int {
 };
 
 // Kernel ids reported by the launch tracer.
+// K_TC_BWD is one backward step: dH and dW of one strip together with the gradient of the next.
 enum KernelId : int {
-  K_TC_FWD = 0, K_TC_BWD_G = 1, K_TC_DH = 2, K_TC_DW = 3,
-  K_SIMT_FWD = 4, K_SIMT_BWD_G = 5, K_SIMT_DH = 6, K_SIMT_DW = 7,
-  K_COMBINE = 8, K_FINALIZE = 9, K_NUM = 10
+  K_TC_FWD = 0, K_TC_BWD = 1,
+  K_SIMT_FWD = 2, K_SIMT_BWD_G = 3, K_SIMT_DH = 4, K_SIMT_DW = 5,
+  K_COMBINE = 6, K_FINALIZE = 7, K_NUM = 8
 };
 
 // Arguments of one strip-GEMM launch (both the tensor-core and the fp32 CUDA-core engines).
@@ -69,6 +70,8 @@ extern int g_inject_stall;
 
 // Tensor-core (tcgen05) engine, bf16 operands: lce_tc.cu
 cudaError_t tc_strip_gemm(const StripArgs& a, cudaStream_t stream, int num_sms);
+// Up to three strip GEMMs in one persistent launch, their tiles scheduled together in order.
+cudaError_t tc_strip_jobs(const StripArgs* jobs, int njobs, cudaStream_t stream, int num_sms);
 // CUDA-core engine, fp32 operands (exact FFMA): lce_simt.cu
 cudaError_t simt_strip_gemm(const StripArgs& a, cudaStream_t stream);
 // Reductions: lce_reduce.cu

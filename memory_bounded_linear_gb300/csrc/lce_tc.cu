@@ -1,10 +1,11 @@
 // Tensor-core strip GEMM engine for bf16 operands on sm_103a (tcgen05 + TMEM + TMA).
 //
-// One persistent, warp-specialised kernel per epilogue mode:
+// One persistent, warp-specialised kernel.  A launch carries up to three GEMM jobs, each with its
+// own epilogue mode, operands and output; its tiles are scheduled together:
 //   warp 0      TMA producer: streams A and B k-blocks (64 bf16 = one 128-byte swizzle span)
-//               into a 4-stage shared-memory ring;
+//               into a shared-memory ring; it also hands out the tiles (dynamic scheduler);
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and one elected
-//               lane issues tcgen05.mma (M=128, N=256, K=16) into the accumulator of the tile;
+//               lane issues tcgen05.mma into the accumulator of the tile;
 //   warps 2..5  epilogue: each thread owns one accumulator row (TMEM lane) and reads its 256
 //               columns 32 at a time with tcgen05.ld, so every per-row reduction of the tile
 //               (max, sum of exp, target gather) is thread-local -- no shuffles are needed.
@@ -15,17 +16,21 @@
 //   DH              A = G_s [N x w] K-major    B = W strip [w x d] MN-major (d contiguous)
 //   DW              A = G_s^T      MN-major    B = H [N x d]       MN-major
 // TMA zero-fills every box element outside the tensor, so ragged M, N and K edges contribute 0
-// to the products; the epilogues mask the columns beyond the strip / vocabulary.
+// to the products; the epilogues mask the columns beyond the strip / vocabulary, and TMA stores
+// clip the output boxes at the edges of their tensors.
 //
-// "Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training", section 3.2 / appendix C: each
-// logit strip is folded into a running per-token state and released; backward recomputes the
-// strip and its gradient.  Here a strip's logits only ever live in TMEM.
+// "Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training", section 3.2 and
+// appendix C: each logit strip is folded into a running per-token state and released; backward
+// recomputes the strip and its gradient.  Here a strip's logits only ever live in TMEM.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <type_traits>
 
 #include "lce_internal.h"
 #include "ptx.cuh"
@@ -47,6 +52,7 @@ constexpr int STAGE_BUF_BYTES = 32 * 128;
 constexpr int STAGING_BYTES = 4 * 2 * STAGE_BUF_BYTES;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // a wait longer than 2 s is treated as a hang
+constexpr int MAX_JOBS = 3;
 
 // Pair tiles per rasterisation group (build-time tunable): more tiles per group re-read the
 // column operand less often but keep a larger row panel live in L2.
@@ -87,29 +93,39 @@ struct Ctl {
 };
 static_assert(sizeof(Ctl) <= CTL_BYTES, "control block too large");
 
-struct KParams {
-  int M, Ncols, K;
+// One GEMM of a launch.
+struct Job {
+  int mode;                           // MODE_*
   int tiles_m, tiles_n, num_tiles, nkb;
-  int b_off;        // FWD/BWD: W row of the strip start; DH: W row (K coordinate) of the strip start
-  int strip_cols;   // FWD/BWD: valid columns of the strip
-  int col0;         // first vocabulary column of the strip
-  float2* part;
-  float* tgt;
+  int b_off;       // FWD/BWD_G: W row of the strip start; DH: W row (K coordinate) of the strip
+  int strip_cols;  // FWD/BWD_G: columns of the strip
+  int col0;        // FWD/BWD_G: first vocabulary column of the strip
+  int c_cols;      // DH/DW: columns of C
+  int accumulate;  // DH: add into C instead of storing
+  int first_strip; // BWD_G: the strip that reports bad labels
+};
+
+struct KParams {
+  Job job[MAX_JOBS];
+  int njobs, total_tiles;
+  int64_t N, V, ignore_index;
+  float2* part;             // FWD: [tiles_n][N] per-(tile, row) (max, sum-exp)
+  float* tgt;               // FWD: [N] target logit
   const int64_t* labels;
-  int64_t V, ignore_index;
-  const float* lse;
-  const float* dloss;
-  const int64_t* n_valid;
+  const float* lse;         // BWD_G
+  const float* dloss;       // BWD_G (null when no job needs it)
+  const int64_t* n_valid;   // BWD_G
   int reduction;
-  __nv_bfloat16* G;
-  int64_t ldg;
-  float* C;
-  int64_t ldc;
-  int accumulate, c_rows, c_cols;
   unsigned* err;
   unsigned* sched;  // [0] next tile ticket, [1] units finished; both zero between launches
-  int first_strip;
   int inject_stall;  // test hook (lce_test_inject_stall): withhold the first k-block
+};
+
+// Per job: A and B operand maps and the map of the epilogue's TMA stores (G strip or C).
+struct TcMaps {
+  CUtensorMap a[MAX_JOBS];
+  CUtensorMap b[MAX_JOBS];
+  CUtensorMap c[MAX_JOBS];
 };
 
 // Bounded wait on an mbarrier phase.  Gives up after WAIT_LIMIT_NS (or at once when another role
@@ -156,11 +172,28 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
   tn = r / gm;
 }
 
+// A scheduler ticket resolved to its job and to the job's row / column tile.
+struct TilePos {
+  int job, tm, tn;
+};
+template <bool PAIR>
+__device__ __forceinline__ TilePos locate(const KParams& p, int t) {
+  int j = 0;
+  while (j + 1 < p.njobs && t >= p.job[j].num_tiles) {
+    t -= p.job[j].num_tiles;
+    ++j;
+  }
+  TilePos r;
+  r.job = j;
+  tile_coords(t, p.job[j].tiles_m, p.job[j].tiles_n, Cfg<PAIR>::RASTER_GROUP, r.tm, r.tn);
+  return r;
+}
+
 // Dynamic tile scheduler.  The producer thread of the (first) CTA takes tickets from a global
-// counter -- tiles come out in raster order, so the tiles in flight at any moment stay together in
-// the raster however unevenly the SMs progress, and operands keep being shared through L2 -- and
-// posts each tile id into the ring `tq` of both CTAs of a pair.  Every other role reads the ids
-// from its own CTA's ring and hands the slot back.  -1 ends the sequence.
+// counter -- tiles come out in job and raster order, so the tiles in flight at any moment stay
+// together however unevenly the SMs progress, and operands keep being shared through L2 -- and
+// posts each ticket into the ring `tq` of both CTAs of a pair.  Every other role reads the
+// tickets from its own CTA's ring and hands the slot back.  -1 ends the sequence.
 template <bool PAIR>
 struct TileQueue {
   Ctl* ctl;
@@ -195,7 +228,7 @@ struct TileQueue {
     return t;
   }
 
-  // Reader: the next tile id of this CTA's ring.  `mask` names the lanes of the calling warp that
+  // Reader: the next ticket of this CTA's ring.  `mask` names the lanes of the calling warp that
   // read it together; the slot is handed back (once per warp) after all of them have.
   __device__ __forceinline__ int take(unsigned mask) {
     const uint32_t full = ptx::smem_addr(&ctl->tq_full[slot]);
@@ -224,16 +257,120 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_base, int k16) {
   return ptx::sw128_desc(tile_base + k16 * 16 * 128, MN_BOX_BYTES, 1024);
 }
 
+// The kernel is compiled per set of modes it may meet (a bit mask of MODE_*): the forward kernel
+// carries only the forward epilogue, the backward kernel the three backward ones.  Keeping the
+// code of each kernel small matters: a kernel carrying all four epilogues ran 13% slower.
+constexpr int MODES_FWD = 1 << MODE_FWD_LSE;
+constexpr int MODES_BWD = (1 << MODE_BWD_G) | (1 << MODE_DH) | (1 << MODE_DW);
+template <int MODES>
+__device__ __forceinline__ constexpr bool has_mode(int m) {
+  return ((MODES >> m) & 1) != 0;
+}
+// The job's mode as the compiler sees it: a constant when the kernel serves a single mode.
+template <int MODES>
+__device__ __forceinline__ int mode_of(const Job& jb) {
+  if constexpr (MODES == MODES_FWD) return MODE_FWD_LSE;
+  else return jb.mode;
+}
+
+// Calls f(integral_constant<int, mode>) for the job's mode, among the modes the kernel serves, so
+// that the per-tile loops below are compiled once per mode with their operand layouts fixed.
+template <int MODES, typename F>
+__device__ __forceinline__ void dispatch_mode(int mode, F&& f) {
+  if constexpr (has_mode<MODES>(MODE_FWD_LSE))
+    if (mode == MODE_FWD_LSE) { f(std::integral_constant<int, MODE_FWD_LSE>{}); return; }
+  if constexpr (has_mode<MODES>(MODE_BWD_G))
+    if (mode == MODE_BWD_G) { f(std::integral_constant<int, MODE_BWD_G>{}); return; }
+  if constexpr (has_mode<MODES>(MODE_DH))
+    if (mode == MODE_DH) { f(std::integral_constant<int, MODE_DH>{}); return; }
+  if constexpr (has_mode<MODES>(MODE_DW))
+    if (mode == MODE_DW) { f(std::integral_constant<int, MODE_DW>{}); return; }
+}
+
+// Position in a shared-memory ring (stage index and phase parity).
+struct Ring {
+  int stage;
+  uint32_t ph;
+};
+
+// Producer side of one tile: its k-blocks of A and B into the stage ring.  False when a wait
+// gave up.  `withhold_first` is the timeout-path test hook.
 template <int MODE, bool PAIR>
-__global__ void __launch_bounds__(THREADS, 1)
-    tc_strip_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const KParams p) {
+__device__ __forceinline__ bool produce_tile(const Job& jb, const CUtensorMap* mA,
+                                             const CUtensorMap* mB, int m0, int n0, uint32_t base,
+                                             Ctl* ctl, Ring& r, volatile int* abort_flag,
+                                             unsigned* err, uint32_t rank, bool withhold_first) {
   using Cf = Cfg<PAIR>;
-  constexpr int STAGES = Cf::STAGES;
-  constexpr int STAGE_BYTES = Cf::STAGE_BYTES;
+  constexpr bool A_MN = (MODE == MODE_DW);
+  constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
+  for (int kb = 0; kb < jb.nkb; ++kb) {
+    const uint32_t empty = ptx::smem_addr(&ctl->empty[r.stage]);
+    const uint32_t full_local = ptx::smem_addr(&ctl->full[r.stage]);
+    if (!wait_bar(empty, r.ph ^ 1u, abort_flag, err)) return false;
+    const uint32_t sa = base + r.stage * Cf::STAGE_BYTES;
+    const uint32_t sb = sa + Cf::A_BYTES;
+    const bool withhold = withhold_first && kb == 0 && r.stage == 0 && r.ph == 0;
+    if (!withhold) {
+      // In a pair every stage's bytes (of both CTAs) are counted on the issuer's barrier.
+      const uint32_t full = PAIR ? ptx::mapa_shared(full_local, 0) : full_local;
+      if (rank == 0) ptx::mbar_arrive_expect_tx(full_local, (PAIR ? 2 : 1) * Cf::STAGE_BYTES);
+      auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
+        if (PAIR) ptx::tma_load_2d_pair(dst, m, x, y, full);
+        else ptx::tma_load_2d(dst, m, x, y, full);
+      };
+      if (A_MN) {
+#pragma unroll
+        for (int c = 0; c < BM / 64; ++c) load(sa + c * MN_BOX_BYTES, mA, m0 + c * 64, kb * BK);
+      } else {
+        load(sa, mA, kb * BK, m0);
+      }
+      if (B_MN) {
+        const int krow = (MODE == MODE_DH ? jb.b_off : 0) + kb * BK;
+#pragma unroll
+        for (int c = 0; c < Cf::B_ROWS / 64; ++c) load(sb + c * MN_BOX_BYTES, mB, n0 + c * 64, krow);
+      } else {
+        load(sb, mB, kb * BK, jb.b_off + n0);
+      }
+    }  // else (test hook): no bytes, no arrival -- the MMA issuer's wait on this stage runs out
+    if (++r.stage == Cf::STAGES) { r.stage = 0; r.ph ^= 1u; }
+  }
+  return true;
+}
+
+// MMA side of one tile: nkb k-blocks of 4 MMAs (K=16 each) into the accumulator at d_tmem.
+template <int MODE, bool PAIR>
+__device__ __forceinline__ bool mma_tile(int nkb, uint32_t d_tmem, uint32_t base, Ctl* ctl, Ring& r,
+                                         volatile int* abort_flag, unsigned* err) {
+  using Cf = Cfg<PAIR>;
   constexpr bool A_MN = (MODE == MODE_DW);
   constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
   constexpr uint32_t IDESC = ptx::idesc_bf16_f32(Cf::TILE_M, BN, A_MN, B_MN);
+  for (int kb = 0; kb < nkb; ++kb) {
+    if (!wait_bar(ptx::smem_addr(&ctl->full[r.stage]), r.ph, abort_flag, err)) return false;
+    ptx::tc_fence_after();
+    const uint32_t sa = base + r.stage * Cf::STAGE_BYTES;
+    const uint32_t sb = sa + Cf::A_BYTES;
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k) {
+      const uint64_t ad = A_MN ? desc_mnmajor(sa, k) : desc_kmajor(sa, k);
+      const uint64_t bd = B_MN ? desc_mnmajor(sb, k) : desc_kmajor(sb, k);
+      if (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+      else ptx::tc_mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+    }
+    // frees the stage (in both CTAs of a pair) once the MMAs have read it
+    if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&ctl->empty[r.stage]), 0x3);
+    else ptx::tc_commit(ptx::smem_addr(&ctl->empty[r.stage]));
+    if (++r.stage == Cf::STAGES) { r.stage = 0; r.ph ^= 1u; }
+  }
+  return true;
+}
+
+template <int MODES, bool PAIR>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_strip_kernel(const __grid_constant__ TcMaps maps, const KParams p) {
+  using Cf = Cfg<PAIR>;
+  constexpr int STAGES = Cf::STAGES;
+  constexpr int STAGE_BYTES = Cf::STAGE_BYTES;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -285,54 +422,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      ptx::prefetch_tmap(&tmA);
-      ptx::prefetch_tmap(&tmB);
+      for (int j = 0; j < p.njobs; ++j) {
+        ptx::prefetch_tmap(&maps.a[j]);
+        ptx::prefetch_tmap(&maps.b[j]);
+      }
       bool ok = true;
-      int stage = 0;
-      uint32_t ph = 0;
+      Ring ring{0, 0u};
       TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u};
       while (ok) {
-        const int tile = (rank == 0) ? tq.post(p.sched, p.num_tiles, units) : tq.take(1u);
+        const int tile = (rank == 0) ? tq.post(p.sched, p.total_tiles, units) : tq.take(1u);
         if (tile < 0) break;
-        int tm, tn;
-        tile_coords(tile, p.tiles_m, p.tiles_n, Cf::RASTER_GROUP, tm, tn);
-        const int m0 = tm * Cf::TILE_M + static_cast<int>(rank) * BM;       // first A row here
-        const int n0 = tn * BN + static_cast<int>(rank) * Cf::B_ROWS * PAIR;  // first B row here
-        for (int kb = 0; kb < p.nkb; ++kb) {
-          const uint32_t empty = ptx::smem_addr(&ctl->empty[stage]);
-          const uint32_t full_local = ptx::smem_addr(&ctl->full[stage]);
-          if (!wait_bar(empty, ph ^ 1u, abort_flag, p.err)) { ok = false; break; }
-          const uint32_t sa = base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + Cf::A_BYTES;
-          if (p.inject_stall && kb == 0 && stage == 0 && ph == 0) {
-            // Test hook: withhold the very first k-block (no bytes, no arrival), so the MMA
-            // issuer's wait on it runs out and the launch takes its timeout path.
-            if (++stage == STAGES) { stage = 0; ph ^= 1u; }
-            continue;
-          }
-          // In a pair every stage's bytes (of both CTAs) are counted on the issuer's barrier.
-          const uint32_t full = PAIR ? ptx::mapa_shared(full_local, 0) : full_local;
-          if (rank == 0) ptx::mbar_arrive_expect_tx(full_local, (PAIR ? 2 : 1) * STAGE_BYTES);
-          auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
-            if (PAIR) ptx::tma_load_2d_pair(dst, m, x, y, full);
-            else ptx::tma_load_2d(dst, m, x, y, full);
-          };
-          if (A_MN) {
-#pragma unroll
-            for (int c = 0; c < BM / 64; ++c) load(sa + c * MN_BOX_BYTES, &tmA, m0 + c * 64, kb * BK);
-          } else {
-            load(sa, &tmA, kb * BK, m0);
-          }
-          if (B_MN) {
-            const int krow = (MODE == MODE_DH ? p.b_off : 0) + kb * BK;
-#pragma unroll
-            for (int c = 0; c < Cf::B_ROWS / 64; ++c)
-              load(sb + c * MN_BOX_BYTES, &tmB, n0 + c * 64, krow);
-          } else {
-            load(sb, &tmB, kb * BK, p.b_off + n0);
-          }
-          if (++stage == STAGES) { stage = 0; ph ^= 1u; }
-        }
+        const TilePos tp = locate<PAIR>(p, tile);
+        const Job& jb = p.job[tp.job];
+        const int m0 = tp.tm * Cf::TILE_M + static_cast<int>(rank) * BM;       // first A row here
+        const int n0 = tp.tn * BN + static_cast<int>(rank) * Cf::B_ROWS * PAIR;  // first B row
+        dispatch_mode<MODES>(mode_of<MODES>(jb), [&](auto m) {
+          ok = produce_tile<decltype(m)::value, PAIR>(jb, &maps.a[tp.job], &maps.b[tp.job], m0, n0,
+                                                      base, ctl, ring, abort_flag, p.err, rank,
+                                                      p.inject_stall != 0);
+        });
       }
       if (!ok) {
         // Let copies already in flight land before the CTA can exit.
@@ -344,39 +452,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && rank == 0) {
       bool ok = true;
-      int stage = 0;
-      uint32_t ph = 0;
+      Ring ring{0, 0u};
       int acc = 0;
       uint32_t aph = 0;
       TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u};
       while (ok) {
-        if (tq.take(1u) < 0) break;
+        const int tile = tq.take(1u);
+        if (tile < 0) break;
+        const TilePos tp = locate<PAIR>(p, tile);
+        const Job& jb = p.job[tp.job];
         if (!wait_bar(ptx::smem_addr(&ctl->tempty[acc]), aph ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.nkb; ++kb) {
-          if (!wait_bar(ptx::smem_addr(&ctl->full[stage]), ph, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t sa = base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + Cf::A_BYTES;
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = A_MN ? desc_mnmajor(sa, k) : desc_kmajor(sa, k);
-            const uint64_t bd = B_MN ? desc_mnmajor(sb, k) : desc_kmajor(sb, k);
-            if (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
-            else ptx::tc_mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
-          }
-          // frees the stage (in both CTAs of a pair) once the MMAs have read it
-          if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&ctl->empty[stage]), 0x3);
-          else ptx::tc_commit(ptx::smem_addr(&ctl->empty[stage]));
-          if (++stage == STAGES) { stage = 0; ph ^= 1u; }
-        }
+        dispatch_mode<MODES>(mode_of<MODES>(jb), [&](auto m) {
+          ok = mma_tile<decltype(m)::value, PAIR>(jb.nkb, d_tmem, base, ctl, ring, abort_flag, p.err);
+        });
         if (!ok) break;
         // accumulator ready for the epilogue warps (of both CTAs of a pair)
         if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&ctl->tfull[acc]), 0x3);
@@ -395,8 +488,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;          // TMEM lane quadrant this warp may access
     const int r_in = q * 32 + lane;  // accumulator row owned by this thread
+    const uint32_t wbuf0 = staging + q * 2 * STAGE_BUF_BYTES;  // this warp's two staging buffers
     float scale_valid = 0.f;
-    if (MODE == MODE_BWD_G) {
+    if (p.dloss != nullptr) {
       const float dl = *p.dloss;
       scale_valid = (p.reduction == 0) ? dl / static_cast<float>(*p.n_valid) : dl;
     }
@@ -406,12 +500,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     while (true) {
       const int tile = tq.take(0xffffffffu);
       if (tile < 0) break;
-      int tm, tn;
-      tile_coords(tile, p.tiles_m, p.tiles_n, Cf::RASTER_GROUP, tm, tn);
+      const TilePos tp = locate<PAIR>(p, tile);
+      const Job& jb = p.job[tp.job];
+      const CUtensorMap* mC = &maps.c[tp.job];
       const uint32_t tfull = ptx::smem_addr(&ctl->tfull[acc]);
       const uint32_t tempty_local = ptx::smem_addr(&ctl->tempty[acc]);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      const int row = tm * Cf::TILE_M + static_cast<int>(rank) * BM + r_in;
+      const int row = tp.tm * Cf::TILE_M + static_cast<int>(rank) * BM + r_in;
+      const int box_row = tp.tm * Cf::TILE_M + static_cast<int>(rank) * BM + q * 32;
       // hand the accumulator back to the MMA issuer (in the pair's first CTA)
       auto release = [&]() {
         ptx::tc_fence_before();
@@ -422,16 +518,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       };
 
-      if (MODE == MODE_FWD_LSE || MODE == MODE_BWD_G) {
-        const bool row_ok = row < p.M;
-        const int tcol0 = tn * BN;
-        const int ncols = min(BN, p.strip_cols - tcol0);  // valid columns of this tile (>= 1)
+      const int mode = mode_of<MODES>(jb);
+      const bool is_fwd = has_mode<MODES>(MODE_FWD_LSE) && mode == MODE_FWD_LSE;
+      const bool is_grad = has_mode<MODES>(MODE_BWD_G) && mode == MODE_BWD_G;
+      if (is_fwd || is_grad) {
+        const bool row_ok = row < p.N;
+        const int tcol0 = tp.tn * BN;
+        const int ncols = min(BN, jb.strip_cols - tcol0);  // valid columns of this tile (>= 1)
         const int64_t y = row_ok ? p.labels[row] : p.ignore_index;
         const bool label_ok = (y != p.ignore_index) && (y >= 0) && (y < p.V);
-        const int64_t trel = y - static_cast<int64_t>(p.col0 + tcol0);
+        const int64_t trel = y - static_cast<int64_t>(jb.col0 + tcol0);
         const int tloc = (label_ok && trel >= 0 && trel < ncols) ? static_cast<int>(trel) : -1;
 
-        if (MODE == MODE_FWD_LSE) {
+        if (is_fwd) {
           float m = -INFINITY, s = 0.f, t = 0.f;
           if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
           ptx::tc_fence_after();
@@ -465,18 +564,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           release();
           if (row_ok) {
-            p.part[static_cast<size_t>(tn) * p.M + row] = make_float2(m, s);
+            p.part[static_cast<size_t>(tp.tn) * p.N + row] = make_float2(m, s);
             if (tloc >= 0) p.tgt[row] = t;
           }
         } else {
           // MODE_BWD_G: G = scale * (exp(Z - lse) - onehot) -> bf16 strip workspace
-          if (row_ok && !label_ok && y != p.ignore_index && p.first_strip && tn == 0)
+          if (row_ok && !label_ok && y != p.ignore_index && jb.first_strip && tp.tn == 0)
             atomicOr(p.err, ERR_LABEL);
           const float scale = label_ok ? scale_valid : 0.f;
           const float nl = label_ok ? -p.lse[row] * LOG2E : 0.f;
-          // The warp's 32 rows go out as 32 x 64-column boxes through two staging buffers.
-          const uint32_t wbuf0 = staging + q * 2 * STAGE_BUF_BYTES;
-          const int box_row = tm * Cf::TILE_M + static_cast<int>(rank) * BM + q * 32;
+          // The warp's 32 rows go out as 32 x 64-column boxes through its two staging buffers.
           if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
           ptx::tc_fence_after();
 #pragma unroll 1
@@ -518,7 +615,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               ptx::fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                ptx::tma_store_2d(&tmC, sbuf, tcol0 + (c - 1) * 32, box_row);
+                ptx::tma_store_2d(mC, sbuf, tcol0 + (c - 1) * 32, box_row);
                 ptx::bulk_commit();
               }
             }
@@ -528,18 +625,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
         }
       } else {
-        // MODE_DH / MODE_DW: C (+)= accumulator, fp32
-        // The warp's 32 rows go out as 32 x 32 fp32 boxes through two staging buffers; the tensor
-        // map clips rows and columns outside C.  Accumulation into dH is a TMA add (one add per
-        // element per launch, in strip order: deterministic).
-        const uint32_t wbuf0 = staging + q * 2 * STAGE_BUF_BYTES;
-        const int box_row = tm * Cf::TILE_M + static_cast<int>(rank) * BM + q * 32;
+        // MODE_DH / MODE_DW: C (+)= accumulator, fp32.  The warp's 32 rows go out as 32 x 32
+        // fp32 boxes through its two staging buffers; the tensor map clips rows and columns
+        // outside C.  Accumulation into dH is a TMA add (one add per element per launch, in
+        // strip order: deterministic).
         if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
         ptx::tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
-          const int col = tn * BN + c * 32;
-          if (col >= p.c_cols) break;  // same for every thread of the CTA
+          const int col = tp.tn * BN + c * 32;
+          if (col >= jb.c_cols) break;  // same for every thread of the CTA
           float v[32];
           ptx::tmem_load32(tbase + c * 32, v);
           const uint32_t sbuf = wbuf0 + (c & 1) * STAGE_BUF_BYTES;
@@ -556,8 +651,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (p.accumulate) ptx::tma_reduce_add_2d(&tmC, sbuf, col, box_row);
-            else ptx::tma_store_2d(&tmC, sbuf, col, box_row);
+            if (jb.accumulate) ptx::tma_reduce_add_2d(mC, sbuf, col, box_row);
+            else ptx::tma_store_2d(mC, sbuf, col, box_row);
             ptx::bulk_commit();
           }
         }
@@ -602,8 +697,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [outer x inner] array with `ld` elements per row,
-// box = [box_outer x box_inner], 128-byte swizzle, zero fill outside the array.
+// 2-D tensor map (bf16, or fp32) over a row-major [outer x inner] array with `ld` elements per
+// row, box = [box_outer x box_inner], 128-byte swizzle, zero fill outside the array.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
               uint32_t box_inner, uint32_t box_outer, int mode, char operand, bool fp32 = false) {
   EncodeTiledFn enc = encode_fn();
@@ -617,9 +712,9 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r =
       enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-          const_cast<void*>(ptr), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+          const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error_detail("tensor map of operand %c, strip GEMM mode %d refused (CUresult %d; %llu x %llu"
                      " elements, row stride %llu, box %u x %u, address %p)",
@@ -631,18 +726,16 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return true;
 }
 
-template <int MODE, bool PAIR>
-cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                        const KParams& p, int grid, cudaStream_t stream) {
+template <int MODES, bool PAIR>
+cudaError_t launch(const TcMaps& maps, const KParams& p, int grid, cudaStream_t stream) {
   using Cf = Cfg<PAIR>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_strip_kernel<MODE, PAIR>,
+    cudaError_t e = cudaFuncSetAttribute(tc_strip_kernel<MODES, PAIR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cf::SMEM_BYTES);
     if (e != cudaSuccess) {
-      set_error_detail("shared-memory attribute of strip GEMM mode %d: %s", MODE,
-                       cudaGetErrorName(e));
+      set_error_detail("shared-memory attribute of the strip GEMM: %s", cudaGetErrorName(e));
       return e;
     }
     attr_set = true;
@@ -661,93 +754,110 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtens
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_strip_kernel<MODE, PAIR>, a, b, c, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_strip_kernel<MODES, PAIR>, maps, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess)
-    set_error_detail("launch of strip GEMM mode %d%s (grid %d, stream %p): %s", MODE,
-                     PAIR ? " (CTA pairs)" : "", grid, static_cast<void*>(stream),
-                     cudaGetErrorName(e));
+    set_error_detail("launch of the strip GEMM (mode %d%s, %d jobs, grid %d, stream %p): %s",
+                     p.job[0].mode, PAIR ? ", CTA pairs" : "", p.njobs, grid,
+                     static_cast<void*>(stream), cudaGetErrorName(e));
   return e;
 }
 
+// Fills job j (maps and tile counts) from one strip GEMM description; false if a map is refused.
 template <bool PAIR>
-cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
+bool make_job(const StripArgs& s, TcMaps& maps, Job& jb, int j) {
   using Cf = Cfg<PAIR>;
-  KParams p{};
-  CUtensorMap ma, mb, mc;  // operands A and B; mc: where the epilogue's TMA stores go
-  bool ok = true;
+  int M, Ncols, K;
+  bool ok;
+  jb = Job{};
+  jb.mode = s.mode;
   switch (s.mode) {
     case MODE_FWD_LSE:
     case MODE_BWD_G:
-      p.M = static_cast<int>(s.N);
-      p.Ncols = s.strip_cols;
-      p.K = static_cast<int>(s.d);
-      p.b_off = s.col0;
-      ok = make_map(&ma, s.H, s.d, s.N, s.d, BK, BM, s.mode, 'A') &&
-           make_map(&mb, s.W, s.d, s.V, s.d, BK, Cf::B_ROWS, s.mode, 'B');
+      M = static_cast<int>(s.N);
+      Ncols = s.strip_cols;
+      K = static_cast<int>(s.d);
+      jb.b_off = s.col0;
+      ok = make_map(&maps.a[j], s.H, s.d, s.N, s.d, BK, BM, s.mode, 'A') &&
+           make_map(&maps.b[j], s.W, s.d, s.V, s.d, BK, Cf::B_ROWS, s.mode, 'B');
       // gradient strip [N x ldg] bf16, written as 64-column x 32-row boxes
-      if (ok) ok = (s.mode == MODE_BWD_G) ? make_map(&mc, s.G, s.ldg, s.N, s.ldg, 64, 32, s.mode, 'G')
-                                         : (mc = ma, true);
+      if (ok && s.mode == MODE_BWD_G)
+        ok = make_map(&maps.c[j], s.G, s.ldg, s.N, s.ldg, 64, 32, s.mode, 'G');
+      else
+        maps.c[j] = maps.a[j];  // unused by the forward epilogue
       break;
     case MODE_DH:
-      p.M = static_cast<int>(s.N);
-      p.Ncols = static_cast<int>(s.d);
-      p.K = s.strip_cols;
-      p.b_off = s.col0;
-      ok = make_map(&ma, s.G, s.ldg, s.N, s.ldg, BK, BM, s.mode, 'A') &&
-           make_map(&mb, s.W, s.d, s.V, s.d, 64, BK, s.mode, 'B') &&
-           make_map(&mc, s.C, s.d, s.N, s.ldc, 32, 32, s.mode, 'C', true);  // dH [N x d] fp32
+      M = static_cast<int>(s.N);
+      Ncols = static_cast<int>(s.d);
+      K = s.strip_cols;
+      jb.b_off = s.col0;
+      ok = make_map(&maps.a[j], s.G, s.ldg, s.N, s.ldg, BK, BM, s.mode, 'A') &&
+           make_map(&maps.b[j], s.W, s.d, s.V, s.d, 64, BK, s.mode, 'B') &&
+           make_map(&maps.c[j], s.C, s.d, s.N, s.ldc, 32, 32, s.mode, 'C', true);  // dH fp32
       break;
     case MODE_DW:
-      p.M = s.strip_cols;
-      p.Ncols = static_cast<int>(s.d);
-      p.K = static_cast<int>(s.N);
-      p.b_off = 0;
-      ok = make_map(&ma, s.G, s.ldg, s.N, s.ldg, 64, BK, s.mode, 'A') &&
-           make_map(&mb, s.H, s.d, s.N, s.d, 64, BK, s.mode, 'B') &&
-           make_map(&mc, s.C, s.d, s.strip_cols, s.ldc, 32, 32, s.mode, 'C', true);  // dW_s
+      M = s.strip_cols;
+      Ncols = static_cast<int>(s.d);
+      K = static_cast<int>(s.N);
+      jb.b_off = 0;
+      ok = make_map(&maps.a[j], s.G, s.ldg, s.N, s.ldg, 64, BK, s.mode, 'A') &&
+           make_map(&maps.b[j], s.H, s.d, s.N, s.d, 64, BK, s.mode, 'B') &&
+           make_map(&maps.c[j], s.C, s.d, s.strip_cols, s.ldc, 32, 32, s.mode, 'C', true);  // dW_s
       break;
     default:
-      return cudaErrorInvalidValue;
+      set_error_detail("unknown strip GEMM mode %d", s.mode);
+      return false;
   }
-  if (!ok) return cudaErrorInvalidResourceHandle;  // the tensor-map encoder refused the operand
-  p.tiles_m = (p.M + Cf::TILE_M - 1) / Cf::TILE_M;
-  p.tiles_n = (p.Ncols + BN - 1) / BN;
-  p.num_tiles = p.tiles_m * p.tiles_n;
-  p.nkb = (p.K + BK - 1) / BK;
-  if (p.num_tiles == 0 || p.nkb == 0) return cudaSuccess;
-  p.strip_cols = s.strip_cols;
-  p.col0 = s.col0;
+  if (!ok) return false;
+  jb.tiles_m = (M + Cf::TILE_M - 1) / Cf::TILE_M;
+  jb.tiles_n = (Ncols + BN - 1) / BN;
+  jb.nkb = (K + BK - 1) / BK;
+  jb.num_tiles = (jb.nkb > 0) ? jb.tiles_m * jb.tiles_n : 0;
+  jb.strip_cols = s.strip_cols;
+  jb.col0 = s.col0;
+  jb.c_cols = s.c_cols;
+  jb.accumulate = s.accumulate;
+  jb.first_strip = s.first_strip;
+  return true;
+}
+
+template <bool PAIR>
+cudaError_t run(const StripArgs* jobs, int njobs, cudaStream_t stream, int num_sms) {
+  TcMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  KParams p{};
+  for (int i = 0; i < njobs; ++i) {
+    Job jb;
+    if (!make_job<PAIR>(jobs[i], maps, jb, p.njobs)) return cudaErrorInvalidResourceHandle;
+    if (jb.num_tiles == 0) continue;  // nothing to compute (e.g. an empty dimension)
+    p.job[p.njobs++] = jb;
+    p.total_tiles += jb.num_tiles;
+  }
+  if (p.njobs == 0) return cudaSuccess;
+  const StripArgs& s = jobs[0];
+  p.N = s.N;
+  p.V = s.V;
+  p.ignore_index = s.ignore_index;
   p.part = s.part;
   p.tgt = s.tgt;
   p.labels = s.labels;
-  p.V = s.V;
-  p.ignore_index = s.ignore_index;
-  p.lse = s.lse;
-  p.dloss = s.dloss;
-  p.n_valid = s.n_valid;
   p.reduction = s.reduction;
-  p.G = static_cast<__nv_bfloat16*>(s.G);
-  p.ldg = s.ldg;
-  p.C = s.C;
-  p.ldc = s.ldc;
-  p.accumulate = s.accumulate;
-  p.c_rows = s.c_rows;
-  p.c_cols = s.c_cols;
   p.err = s.err;
-  p.first_strip = s.first_strip;
+  for (int i = 0; i < njobs; ++i)
+    if (jobs[i].mode == MODE_BWD_G) {
+      p.lse = jobs[i].lse;
+      p.dloss = jobs[i].dloss;
+      p.n_valid = jobs[i].n_valid;
+    }
   p.sched = s.err + WS_SCHED_WORD;
   p.inject_stall = g_inject_stall;  // one launch only
   g_inject_stall = 0;
   // persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than there are tiles
   const int units = PAIR ? num_sms / 2 : num_sms;
-  const int grid = (p.num_tiles < units ? p.num_tiles : units) * (PAIR ? 2 : 1);
-  switch (s.mode) {
-    case MODE_FWD_LSE: return launch_mode<MODE_FWD_LSE, PAIR>(ma, mb, mc, p, grid, stream);
-    case MODE_BWD_G: return launch_mode<MODE_BWD_G, PAIR>(ma, mb, mc, p, grid, stream);
-    case MODE_DH: return launch_mode<MODE_DH, PAIR>(ma, mb, mc, p, grid, stream);
-    default: return launch_mode<MODE_DW, PAIR>(ma, mb, mc, p, grid, stream);
-  }
+  const int grid = (p.total_tiles < units ? p.total_tiles : units) * (PAIR ? 2 : 1);
+  // a launch never mixes the forward with the backward
+  return (p.job[0].mode == MODE_FWD_LSE) ? launch<MODES_FWD, PAIR>(maps, p, grid, stream)
+                                          : launch<MODES_BWD, PAIR>(maps, p, grid, stream);
 }
 
 }  // namespace
@@ -755,14 +865,23 @@ cudaError_t run(const StripArgs& s, cudaStream_t stream, int num_sms) {
 int g_tile_config = 0;
 int g_inject_stall = 0;
 
-cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) {
+cudaError_t tc_strip_jobs(const StripArgs* jobs, int njobs, cudaStream_t stream, int num_sms) {
+  if (njobs < 1 || njobs > MAX_JOBS) return cudaErrorInvalidValue;
   // Rows of C: tokens for the logit, gradient and dH GEMMs, strip columns for dW.
-  const int64_t rows = (s.mode == MODE_DW) ? s.strip_cols : s.N;
+  int64_t rows = 0;
+  for (int i = 0; i < njobs; ++i) {
+    const int64_t r = (jobs[i].mode == MODE_DW) ? jobs[i].strip_cols : jobs[i].N;
+    rows = r > rows ? r : rows;
+  }
   bool pair;
   if (g_tile_config == 1) pair = false;
   else if (g_tile_config == 2) pair = true;
   else pair = rows > BM;  // pairs need a second 128-row half to be worth launching
-  return pair ? run<true>(s, stream, num_sms) : run<false>(s, stream, num_sms);
+  return pair ? run<true>(jobs, njobs, stream, num_sms) : run<false>(jobs, njobs, stream, num_sms);
+}
+
+cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) {
+  return tc_strip_jobs(&s, 1, stream, num_sms);
 }
 
 }  // namespace lce

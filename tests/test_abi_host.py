@@ -33,7 +33,7 @@ def test_status_strings_and_kernel_names(lib):
         assert s and s != b"unknown status", name
     assert lib.lce_status_string(99) == b"unknown status"
     assert lib.lce_kernel_name(0) == b"tc_fwd_lse"
-    assert lib.lce_kernel_name(3) == b"tc_dw"
+    assert lib.lce_kernel_name(1) == b"tc_bwd"
     assert lib.lce_kernel_name(-1) is None and lib.lce_kernel_name(1000) is None
 
 
@@ -42,16 +42,19 @@ def _ws(lib, N, d, V, s, dt=0):
 
 
 def test_workspace_size_formula(lib):
-    # bf16: header + max(forward state, one strip of bf16 gradient rows padded to 256 columns)
+    # bf16, large backward step (128 x 24 dH tiles > 512): header + max(forward state, one strip
+    # of bf16 gradient rows padded to 256 columns)
     N, d, V, s = 32768, 6144, 151552, 16384
     g_bytes = N * 16384 * 2
     assert _ws(lib, N, d, V, s) == 256 + g_bytes
-    # fp32 engine: 64-wide tiles, fp32 gradient strip
+    # bf16, small backward step (16 x 8 dH tiles): two gradient strips, consecutive strips overlap
+    assert _ws(lib, 4096, 2048, 151936, 8192) == 256 + 2 * 4096 * 8192 * 2
+    # fp32 engine: 64-wide tiles, one fp32 gradient strip
     assert _ws(lib, 256, 256, 4096, 512, 1) == 256 + 256 * 512 * 4
     # strip wider than V: the strip is V wide (padded to the tile width)
     assert _ws(lib, 100, 64, 300, 4096) == 256 + max(
         ((100 * 8 + 255) // 256 * 256) + ((100 * 4 + 255) // 256 * 256) + ((2 * 100 * 8 + 255) // 256 * 256),
-        (100 * 512 * 2 + 255) // 256 * 256)
+        2 * ((100 * 512 * 2 + 255) // 256 * 256))
 
 
 def test_workspace_is_bounded_by_strip_not_vocab(lib):

@@ -93,7 +93,7 @@ def test_strip_width_invariance(cuda_lib, strip):
 
 @pytest.mark.parametrize("w", [
     W4.with_sizes(N=300, d=64, V=40000, strip_V=128),
-    W4.with_sizes(N=1000, d=128, V=70000, strip_V=1024),
+    W4.with_sizes(N=1000, d=128, V=70000, strip_V=512),
     WT.with_sizes(N=64, d=32, V=5000, strip_V=128),
 ], ids=["bf16-strip128", "bf16-strip1024", "f32-strip128"])
 def test_forward_strip_by_strip(cuda_lib, w):
