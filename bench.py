@@ -348,7 +348,13 @@ def main():
     dominant = max((k for k in agg if k in GEMM_FLOP_FACTOR), key=lambda k: agg[k][1])
     n_launch, t_kernel = agg[dominant]
     peaks, peak_src = measured_peaks()
-    peak_tf = peaks["bf16_tflops_sustained"] if w.dtype == "bf16" else None
+    if w.dtype == "bf16":
+        peak_tf, peak_name = peaks["bf16_tflops_sustained"], f"bf16_tflops_sustained ({peak_src})"
+    else:
+        # exact fp32 runs on the FFMA units: 152 SMs x 128 fp32 lanes x 2 FLOP x max SM clock
+        mhz = peaks.get("sm_max_mhz", 2070.0)
+        peak_tf = 152 * 128 * 2 * mhz * 1e6 / 1e12
+        peak_name = f"derived fp32 FFMA peak: 152 SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz"
     # algorithmic FLOPs of that kernel per step: factor * N * d * V (2 per contraction it runs,
     # summed over its launches -- every strip, tail strip included)
     kernel_flops_step = GEMM_FLOP_FACTOR[dominant] * N * d * V
@@ -358,7 +364,7 @@ def main():
                 "unit": "TFLOP/s", "frac": (achieved / peak_tf) if peak_tf else None,
                 "traffic": measured_traffic(w.name, S, dominant), "launches": n_launch,
                 "avg_launch_ms": t_kernel / n_launch,
-                "peak_source": f"bf16_tflops_sustained ({peak_src})",
+                "peak_source": peak_name,
                 "per_kernel_ms_per_step": {k: v[1] / args.steps for k, v in sorted(agg.items())}}
     clk = clocks.summary()
 

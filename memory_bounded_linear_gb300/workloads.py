@@ -85,6 +85,11 @@ WORKLOADS = {
         Workload("n32768-d6144-v151552-outliers", N=32768, d=6144, V=151552, strip_V=16384,
                  dtype="bf16", h_scale=0.5, labels="zipf", outlier_frac=0.01,
                  reduction="sum"),
+        # The shape the Ring-DTP benchmark times in FP32 ("Flattening Every Memory Peak",
+        # appendix C: N = 16,384, H = 7,168, V = 200,000); the pages give no distributions, so
+        # the plain ones: H ~ N(0,1), W ~ N(0,1/d), uniform labels, mean reduction.
+        Workload("n16384-d7168-v200000-fp32", N=16384, d=7168, V=200000, strip_V=16384,
+                 dtype="f32"),
     ]
 }
 

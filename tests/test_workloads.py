@@ -9,7 +9,7 @@ from memory_bounded_linear_gb300.workloads import (IGNORE_INDEX, WORKLOADS, make
                                                    zipf_ranks)
 
 
-def test_five_workloads_with_stated_sizes():
+def test_workloads_with_stated_sizes():
     sizes = {(w.N, w.d, w.V, w.strip_V, w.dtype, w.reduction) for w in WORKLOADS.values()}
     assert sizes == {
         (256, 256, 4096, 512, "f32", "mean"),
@@ -17,6 +17,8 @@ def test_five_workloads_with_stated_sizes():
         (16384, 4096, 131072, 16384, "bf16", "mean"),
         (65536, 2048, 151936, 8192, "bf16", "mean"),
         (32768, 6144, 151552, 16384, "bf16", "sum"),
+        # the pages' FP32 benchmark shape (Ring-DTP, appendix C)
+        (16384, 7168, 200000, 16384, "f32", "mean"),
     }
     assert WORKLOADS["n65536-d2048-v151936"].strip_sweep == (4096, 8192, 16384, 32768)
 
