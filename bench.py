@@ -65,17 +65,22 @@ def tokens_per_second(world: int, tokens_per_rank: int, ms_per_step: float) -> f
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each tensor-core
 # kernel, from one ncu capture of this benchmark's timed step at full size (one pass per
-# kernel), keyed by workload, strip width and kernel.  They describe the kernel source whose
+# kernel), keyed by workload, strip width, kernel and arithmetic.  They describe the source whose
 # SHA-256 is KERNEL_SOURCE_SHA256; once the source differs they no longer apply (traffic: null).
 KERNEL_SOURCES = ("memory_bounded_linear_gb300/csrc/lce_tc.cu",
                   "memory_bounded_linear_gb300/csrc/ptx.cuh",
                   "memory_bounded_linear_gb300/csrc/lce_internal.h")
-KERNEL_SOURCE_SHA256 = "16ebca2de2dd622cf8dfeeff9197b68826be173714653b86c7aeb317bfe8071a"
+KERNEL_SOURCE_SHA256 = "db13303ca53408257f62f7ca3cec55d05c602f417e9325dceafb056cd90d1b2e"
 MEASURED_TRAFFIC = {
     # N=32768 d=6144 V=151552, strip 16384: the timed step's 31 launches -- the forward over the
     # whole vocabulary, then per strip the gradient, dH and dW launches (averaged over the 30)
-    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse"): 30413200640,
-    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd"): 7303313442,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse", "bf16"): 30417206016,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd", "bf16"): 7725515963,
+    # N=16384 d=7168 V=200000 fp32, three-product tf32, strip 16384: the timed step's 39
+    # tensor-core launches -- 13 forward strips, then per strip the gradient launch and the
+    # dH + dW launch (averaged over the 26)
+    ("n16384-d7168-v200000-fp32", 16384, "tc_fwd_lse", "tf32x3"): 14371110971,
+    ("n16384-d7168-v200000-fp32", 16384, "tc_bwd", "tf32x3"): 30438687379,
 }
 
 
@@ -88,11 +93,11 @@ def kernel_source_sha256() -> str:
     return h.hexdigest()
 
 
-def measured_traffic(workload: str, strip_V: int, kernel: str):
+def measured_traffic(workload: str, strip_V: int, kernel: str, dtype: str):
     """Bytes per launch measured for this kernel source, else None."""
     if KERNEL_SOURCE_SHA256 is None or kernel_source_sha256() != KERNEL_SOURCE_SHA256:
         return None
-    return MEASURED_TRAFFIC.get((workload, strip_V, kernel))
+    return MEASURED_TRAFFIC.get((workload, strip_V, kernel, dtype))
 
 
 def measured_peaks():
@@ -184,10 +189,14 @@ def cpu_baseline(w, H, W, y, target_s=15.0, min_tokens=16):
         oracle.token_block_fwd_bwd(Hb, Wn, yb, scale)
         return time.perf_counter() - t0
 
+    # grow the sample until it takes at least 2/3 of target_s (the first, small runs also warm up
+    # the BLAS thread pool), never beyond the batch
     n = min_tokens
     t = run(n)
-    if t < target_s / 4:
-        n = int(min(w.N, max(n, n * target_s / max(t, 1e-3) / 1.5)))
+    for _ in range(3):
+        if t >= target_s * 2 / 3 or n >= w.N:
+            break
+        n = int(min(w.N, max(n + 1, n * target_s / max(t, 1e-3))))
         t = run(n)
     cores = len(os.sched_getaffinity(0))
     threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", cores)))
@@ -248,12 +257,19 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--tile-config", type=int, default=0, choices=[0, 1, 2],
                     help="tensor-core tile variant: 0 automatic, 1 single-CTA, 2 CTA pairs")
+    ap.add_argument("--f32-mode", dest="f32_mode", default="exact", choices=["exact", "tf32x3"],
+                    help="arithmetic for fp32 workloads: exact FFMA, or three tf32 tensor-core "
+                         "products per fp32 product")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override N (same d, V, strip and distributions; for small profiling runs)")
+    ap.add_argument("--vocab", type=int, default=None,
+                    help="override V (same N, d, strip and distributions; for small profiling runs)")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
     if args.tokens:
         w = w.with_sizes(N=args.tokens)
+    if args.vocab:
+        w = w.with_sizes(V=args.vocab)
     args.strip_V = args.strip_V or w.strip_V
     if args.warmup < 3:
         args.warmup = 3
@@ -273,8 +289,10 @@ def main():
     _lib.check(lib.lce_set_tile_config(args.tile_config), "lce_set_tile_config")
 
     N, d, V, S = w.N, w.d, w.V, args.strip_V
+    fm = args.f32_mode
+    dt = "tf32x3" if (w.dtype == "f32" and fm == "tf32x3") else w.dtype
     H, W, y = make_inputs(w, dev, seed=rank)
-    ws_bytes = api.lce_workspace_size(N, d, V, S, w.dtype)
+    ws_bytes = api.lce_workspace_size(N, d, V, S, dt)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     loss = torch.empty((), device=dev)
     lse = torch.empty(N, device=dev)
@@ -286,9 +304,9 @@ def main():
 
     def step():
         api.lce_forward(H, W, y, strip_V=S, reduction=w.reduction, workspace=ws,
-                        out=(loss, lse, nv), stream=stream)
+                        out=(loss, lse, nv), stream=stream, f32_mode=fm)
         api.lce_backward(H, W, y, lse, nv, one, strip_V=S, reduction=w.reduction, workspace=ws,
-                         dH=dH, dW=dW, stream=stream)
+                         dH=dH, dW=dW, stream=stream, f32_mode=fm)
 
     def barrier():
         if world > 1:
@@ -307,7 +325,7 @@ def main():
     peak = torch.cuda.max_memory_allocated(dev)
 
     # per-launch trace buffers (events recorded around every launch on the launching stream)
-    per_step = 2 * ((V + S - 1) // S) + 1 + 3 * ((V + S - 1) // S)
+    per_step = 7 * ((V + S - 1) // S) + 4  # at most: splits, GEMMs, combines, finalize
     cap = per_step * args.steps + 16
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
     stops = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
@@ -348,8 +366,16 @@ def main():
     dominant = max((k for k in agg if k in GEMM_FLOP_FACTOR), key=lambda k: agg[k][1])
     n_launch, t_kernel = agg[dominant]
     peaks, peak_src = measured_peaks()
-    if w.dtype == "bf16":
+    # three-product tf32: the tensor pipe runs three tf32 products per fp32 product, so the
+    # kernel's tensor work is 3x its fp32 GEMM FLOPs, set against the tf32 peak (the measured bf16
+    # peak x the nominal dense tf32 / bf16 ratio, 18 / 36 PFLOP/s per 8 GPUs)
+    x3_factor = 3 if dt == "tf32x3" else 1
+    if dt == "bf16":
         peak_tf, peak_name = peaks["bf16_tflops_sustained"], f"bf16_tflops_sustained ({peak_src})"
+    elif dt == "tf32x3":
+        peak_tf = peaks["bf16_tflops_sustained"] * 0.5
+        peak_name = (f"tf32 dense = bf16_tflops_sustained ({peak_src}) x nominal tf32/bf16 "
+                     "ratio 0.5")
     else:
         # exact fp32 runs on the FFMA units: 152 SMs x 128 fp32 lanes x 2 FLOP x max SM clock
         mhz = peaks.get("sm_max_mhz", 2070.0)
@@ -357,16 +383,28 @@ def main():
         peak_name = f"derived fp32 FFMA peak: 152 SMs x 128 lanes x 2 FLOP x {mhz:.0f} MHz"
     # algorithmic FLOPs of that kernel per step: factor * N * d * V (2 per contraction it runs,
     # summed over its launches -- every strip, tail strip included)
-    kernel_flops_step = GEMM_FLOP_FACTOR[dominant] * N * d * V
+    kernel_flops_step = GEMM_FLOP_FACTOR[dominant] * N * d * V * x3_factor
     achieved = kernel_flops_step * args.steps / (t_kernel / 1e3) / 1e12
-    roofline = {"kernel": dominant, "bound": "tensor" if w.dtype == "bf16" else "alu",
+    roofline = {"kernel": dominant, "bound": "alu" if dt == "f32" else "tensor",
                 "achieved": achieved, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": (achieved / peak_tf) if peak_tf else None,
-                "traffic": measured_traffic(w.name, S, dominant), "launches": n_launch,
+                "traffic": (None if (args.tokens or args.vocab)
+                            else measured_traffic(w.name, S, dominant, dt)),
+                "launches": n_launch,
                 "avg_launch_ms": t_kernel / n_launch,
                 "peak_source": peak_name,
                 "per_kernel_ms_per_step": {k: v[1] / args.steps for k, v in sorted(agg.items())}}
     clk = clocks.summary()
+    if dt != "f32" and clk.get("sm_mhz") and clk.get("samples", 0) >= 10:
+        # Context for the fraction above: the dense tensor rate per SM and clock (8192 bf16 or
+        # 4096 tf32 FLOP per cycle, the per-SM rate behind the nominal 2.25 / 1.1 PFLOP/s) at the
+        # median SM clock sampled during the timed region.  Under the power cap the tf32 MMAs hold
+        # a higher clock than the bf16 GEMMs behind the measured peak, so against that peak x 0.5
+        # a tf32 kernel can read above 1.  Only with at least 10 clock samples (2 s of timed work).
+        per_clk = 8192 if dt == "bf16" else 4096
+        p_clk = 152 * per_clk * clk["sm_mhz"] * 1e6 / 1e12
+        roofline["peak_at_sampled_clock"] = p_clk
+        roofline["frac_at_sampled_clock"] = achieved / p_clk
 
     # End to end through the public API: every step copies its inputs (H, W, labels) from pinned
     # host memory to the device, runs forward+backward and reads the loss back to the host.  The
@@ -397,9 +435,9 @@ def main():
             stream.wait_event(copied[b])
             Hd, Wd, yd = bufs[b]
             api.lce_forward(Hd, Wd, yd, strip_V=S, reduction=w.reduction, workspace=ws,
-                            out=(loss, lse, nv), stream=stream)
+                            out=(loss, lse, nv), stream=stream, f32_mode=fm)
             api.lce_backward(Hd, Wd, yd, lse, nv, one, strip_V=S, reduction=w.reduction,
-                             workspace=ws, dH=dH, dW=dW, stream=stream)
+                             workspace=ws, dH=dH, dW=dW, stream=stream, f32_mode=fm)
             consumed[b].record(stream)
             loss_h[b].copy_(loss, non_blocking=True)
 
@@ -437,14 +475,14 @@ def main():
             "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.dtype, "data": "synthetic",
+            "dtype": dt, "data": "synthetic",
             "config": {"workload": w.name, "N": N, "d": d, "V": V, "strip_V": S,
                        "reduction": w.reduction, "parallelism": f"independent batch per GPU x{world}",
                        "tile_config": ["auto", "single-cta", "cta-pair"][args.tile_config],
                        "l2": "inputs larger than L2 (H+W = %.0f MB > 129 MB), no flush"
                              % ((H.numel() * H.element_size() + W.numel() * W.element_size()) / 1e6)},
             "tflops": tflops,
-            "frac_of_peak": tflops / peak_tf if peak_tf else None,
+            "frac_of_peak": x3_factor * tflops / peak_tf if peak_tf else None,
             "peak_mb": peak / 1e6,
             "peak_minus_inputs_outputs_mb": (peak - in_out_bytes) / 1e6,
             "workspace_mb": ws_bytes / 1e6,

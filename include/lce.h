@@ -20,7 +20,8 @@
  *
  * Conventions shared by every entry point
  *   - All tensor arguments are DEVICE pointers to dense row-major arrays on the current device.
- *     H and W hold bf16 (LCE_BF16) or fp32 (LCE_F32) values; dH and dW are always fp32.
+ *     H and W hold bf16 (LCE_BF16) or fp32 (LCE_F32, LCE_F32_TF32X3) values; dH and dW are
+ *     always fp32.
  *     labels are int64.  Every pointer must be 16-byte aligned.
  *   - stream is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every call
  *     only enqueues work on that stream and returns; nothing is synchronised except in
@@ -61,7 +62,18 @@ typedef enum {
 } lce_status_t;
 
 typedef enum { LCE_REDUCTION_MEAN = 0, LCE_REDUCTION_SUM = 1 } lce_reduction_t;
-typedef enum { LCE_BF16 = 0, LCE_F32 = 1 } lce_dtype_t;
+/*
+ * Input format and arithmetic.
+ *   LCE_BF16        bf16 H and W; tensor-core products, fp32 accumulation.
+ *   LCE_F32         fp32 H and W; exact fp32 products and sums on the CUDA cores.
+ *   LCE_F32_TF32X3  fp32 H and W on the tensor cores: every operand x is split into tf32 parts
+ *                   hi = nearest tf32 of x and lo = nearest tf32 of (x - hi), and every product is
+ *                   formed as hi*hi' + hi*lo' + lo*hi' with fp32 accumulation (the dropped lo*lo'
+ *                   and the rounding of lo are about 2^-21 relative): about fp32 accuracy at
+ *                   tensor-core speed.
+ * dH and dW are fp32 in every format.
+ */
+typedef enum { LCE_BF16 = 0, LCE_F32 = 1, LCE_F32_TF32X3 = 2 } lce_dtype_t;
 
 /*
  * Bytes of device workspace that lce_forward and lce_backward need for these sizes; 0 when the
@@ -73,7 +85,11 @@ typedef enum { LCE_BF16 = 0, LCE_F32 = 1 } lce_dtype_t;
  * per-tile partial states of one strip) and the backward region: one strip of the logit gradient
  * (N x strip_V elements of the input dtype), or two for bf16 when the backward of a strip is small
  * (ceil(N/256) * ceil(d/256) <= 512): each backward launch then overlaps dH and dW of one strip
- * with the gradient of the next.
+ * with the gradient of the next.  LCE_F32_TF32X3 places the tf32 hi and lo parts of H (2 x N x d
+ * fp32) and of one W strip (2 x min(strip_V, V) x d fp32) after the header, and its backward
+ * region holds, as hi and lo parts each, H and the W strip transposed, the gradient strip
+ * (N x strip_V fp32) and the gradient strip transposed: the tf32 MMAs read every operand with
+ * the contracted index contiguous.
  */
 size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dtype);
 

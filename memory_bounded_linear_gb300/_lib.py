@@ -19,7 +19,7 @@ STATUS_NAMES = {
     6: "LCE_ERR_TIMEOUT", 7: "LCE_ERR_UNSUPPORTED_DEVICE",
 }
 REDUCTIONS = {"mean": 0, "sum": 1}
-DTYPES = {"bf16": 0, "f32": 1}
+DTYPES = {"bf16": 0, "f32": 1, "tf32x3": 2}
 
 _c_i64 = ctypes.c_int64
 _c_p = ctypes.c_void_p

@@ -15,13 +15,19 @@ import torch
 from . import _lib
 
 _DT = {torch.bfloat16: "bf16", torch.float32: "f32"}
+# Arithmetic for float32 inputs: "exact" fp32 products on the CUDA cores (LCE_F32), or "tf32x3"
+# on the tensor cores, each product from three tf32 products of hi / lo parts (LCE_F32_TF32X3).
+F32_MODES = {"exact": "f32", "tf32x3": "tf32x3"}
 
 
-def _dtype_name(t: torch.Tensor) -> str:
+def _dtype_name(t: torch.Tensor, f32_mode: str = "exact") -> str:
     try:
-        return _DT[t.dtype]
+        dt = _DT[t.dtype]
     except KeyError:
         raise TypeError(f"H and W must be bfloat16 or float32, got {t.dtype}") from None
+    if f32_mode not in F32_MODES:
+        raise ValueError(f"f32_mode must be one of {sorted(F32_MODES)}, got {f32_mode!r}")
+    return F32_MODES[f32_mode] if dt == "f32" else dt
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -56,14 +62,15 @@ def lce_workspace_size(N: int, d: int, V: int, strip_V: int, dtype: str = "bf16"
 
 def lce_forward(H, W, labels, *, ignore_index: int = -100, strip_V: int = 8192,
                 reduction: str = "mean", workspace: Optional[torch.Tensor] = None,
-                stream: Optional[torch.cuda.Stream] = None, out=None):
+                stream: Optional[torch.cuda.Stream] = None, out=None, f32_mode: str = "exact"):
     """Run the forward entry point.  Returns (loss [] fp32, lse [N] fp32, n_valid [] int64,
-    workspace).  ``out`` may supply preallocated (loss, lse, n_valid)."""
+    workspace).  ``out`` may supply preallocated (loss, lse, n_valid); ``f32_mode`` picks the
+    arithmetic for float32 inputs ("exact" or "tf32x3")."""
     _check_inputs(H, W, labels)
     lib = _lib.load()
     N, d = H.shape
     V = W.shape[0]
-    dt = _dtype_name(H)
+    dt = _dtype_name(H, f32_mode)
     ws_bytes = lce_workspace_size(N, d, V, strip_V, dt)
     if ws_bytes == 0:
         raise _lib.LceError(2, "lce_workspace_size")
@@ -88,13 +95,13 @@ def lce_forward(H, W, labels, *, ignore_index: int = -100, strip_V: int = 8192,
 def lce_backward(H, W, labels, lse, n_valid, dloss, *, ignore_index: int = -100,
                  strip_V: int = 8192, reduction: str = "mean",
                  workspace: Optional[torch.Tensor] = None, dH=None, dW=None,
-                 stream: Optional[torch.cuda.Stream] = None):
+                 stream: Optional[torch.cuda.Stream] = None, f32_mode: str = "exact"):
     """Run the backward entry point.  Returns (dH [N, d] fp32, dW [V, d] fp32, workspace)."""
     _check_inputs(H, W, labels)
     lib = _lib.load()
     N, d = H.shape
     V = W.shape[0]
-    dt = _dtype_name(H)
+    dt = _dtype_name(H, f32_mode)
     ws_bytes = lce_workspace_size(N, d, V, strip_V, dt)
     if ws_bytes == 0:
         raise _lib.LceError(2, "lce_workspace_size")
@@ -131,25 +138,27 @@ class LinearCrossEntropy(torch.autograd.Function):
     """loss = CE(H W^T, labels) without the N x V logits; gradients for H and W."""
 
     @staticmethod
-    def forward(ctx, H, W, labels, ignore_index, strip_V, reduction):
+    def forward(ctx, H, W, labels, ignore_index, strip_V, reduction, f32_mode):
         loss, lse, n_valid, ws = lce_forward(H, W, labels, ignore_index=ignore_index,
-                                             strip_V=strip_V, reduction=reduction)
+                                             strip_V=strip_V, reduction=reduction,
+                                             f32_mode=f32_mode)
         del ws  # the forward workspace is released before backward allocates its own
         ctx.save_for_backward(H, W, labels, lse, n_valid)
-        ctx.cfg = (ignore_index, strip_V, reduction)
+        ctx.cfg = (ignore_index, strip_V, reduction, f32_mode)
         return loss
 
     @staticmethod
     def backward(ctx, dloss):
         H, W, labels, lse, n_valid = ctx.saved_tensors
-        ignore_index, strip_V, reduction = ctx.cfg
+        ignore_index, strip_V, reduction, f32_mode = ctx.cfg
         dH, dW, _ = lce_backward(H, W, labels, lse, n_valid, dloss, ignore_index=ignore_index,
-                                 strip_V=strip_V, reduction=reduction)
-        return dH.to(H.dtype), dW.to(W.dtype), None, None, None, None
+                                 strip_V=strip_V, reduction=reduction, f32_mode=f32_mode)
+        return dH.to(H.dtype), dW.to(W.dtype), None, None, None, None, None
 
 
 def linear_cross_entropy(H, W, labels, ignore_index: int = -100, strip_V: int = 8192,
-                         reduction: str = "mean"):
+                         reduction: str = "mean", f32_mode: str = "exact"):
     """Fused vocabulary projection + cross-entropy (autograd).  H [N, d], W [V, d] (bf16 or fp32),
-    labels [N] int64; returns the fp32 scalar loss."""
-    return LinearCrossEntropy.apply(H, W, labels, ignore_index, strip_V, reduction)
+    labels [N] int64; returns the fp32 scalar loss.  ``f32_mode`` ("exact" or "tf32x3") picks the
+    arithmetic for float32 inputs."""
+    return LinearCrossEntropy.apply(H, W, labels, ignore_index, strip_V, reduction, f32_mode)

@@ -29,8 +29,15 @@ struct Layout {
   int64_t ldg;      // row stride of the strip gradient workspace (elements)
   int tiles;        // logit tiles per full strip
   size_t off_run, off_tgt, off_part, off_g;
-  size_t g_bytes;   // one gradient strip
+  size_t g_bytes;   // one gradient strip (LCE_F32_TF32X3: its hi part; the lo part follows)
   bool overlap_bwd; // two gradient strips: each backward launch also computes the next gradient
+  // LCE_F32_TF32X3 only: tf32 hi / lo parts, each at off_* with its lo part *_part bytes later
+  size_t off_h, h_part;    // H [N x d]
+  size_t off_w, w_part;    // one strip of W [w x d]
+  size_t off_ht, ht_part;  // H^T [d x ldt]              (backward)
+  size_t off_wt, wt_part;  // the W strip transposed [d x ldg]   (backward)
+  size_t off_gt, gt_part;  // the gradient strip transposed [ldg x ldt] (backward)
+  int64_t ldt;             // N rounded up to a multiple of 32
   size_t total;
 };
 
@@ -44,25 +51,50 @@ bool shape_ok(int64_t N, int64_t d, int64_t V, int64_t strip_V) {
 
 bool make_layout(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dt, Layout* L) {
   if (!shape_ok(N, d, V, strip_V)) return false;
-  if (dt != LCE_BF16 && dt != LCE_F32) return false;
-  L->bn = (dt == LCE_BF16) ? TC_BN : SIMT_BN;
+  if (dt != LCE_BF16 && dt != LCE_F32 && dt != LCE_F32_TF32X3) return false;
+  const bool x3 = (dt == LCE_F32_TF32X3);
+  *L = Layout{};
+  L->bn = (dt == LCE_F32) ? SIMT_BN : TC_BN;
   L->w = std::min(strip_V, V);
   L->ldg = (L->w + L->bn - 1) / L->bn * L->bn;
   L->tiles = static_cast<int>((L->w + L->bn - 1) / L->bn);
+  L->ldt = (N + 31) / 32 * 32;
   const size_t n = static_cast<size_t>(N);
+  const size_t dd = static_cast<size_t>(d);
   const size_t elt = (dt == LCE_BF16) ? 2 : 4;
-  L->off_run = WS_HEADER_BYTES;
+  size_t base = WS_HEADER_BYTES;
+  if (x3) {  // split operands of both directions: H once per call, W one strip at a time
+    L->h_part = align256(n * dd * 4);
+    L->w_part = align256(static_cast<size_t>(L->w) * dd * 4);
+    L->off_h = base;
+    L->off_w = L->off_h + 2 * L->h_part;
+    base = L->off_w + 2 * L->w_part;
+  }
+  L->off_run = base;
   L->off_tgt = L->off_run + align256(n * sizeof(float2));
   L->off_part = L->off_tgt + align256(n * sizeof(float));
   const size_t fwd_end = L->off_part + align256(static_cast<size_t>(L->tiles) * n * sizeof(float2));
-  L->off_g = WS_HEADER_BYTES;
   L->g_bytes = align256(n * static_cast<size_t>(L->ldg) * elt);
-  // A small backward step (dH of one strip: few 256 x 256 tiles, a launch of a few waves) runs
-  // overlapped with the next strip's gradient in one launch, which needs a second gradient strip;
-  // a large one fills the GPU by itself and keeps the single strip.
-  const int64_t dh_tiles = ((N + 255) / 256) * ((d + 255) / 256);
-  L->overlap_bwd = (dt == LCE_BF16) && dh_tiles <= kOverlapMaxTiles;
-  const size_t bwd_end = L->off_g + (L->overlap_bwd ? 2 : 1) * L->g_bytes;
+  size_t bwd_end;
+  if (x3) {
+    // transposed parts for the K-major tf32 MMAs of dH and dW, then G and G^T (hi, lo each)
+    L->ht_part = align256(dd * static_cast<size_t>(L->ldt) * 4);
+    L->wt_part = align256(dd * static_cast<size_t>(L->ldg) * 4);
+    L->gt_part = align256(static_cast<size_t>(L->ldg) * static_cast<size_t>(L->ldt) * 4);
+    L->off_ht = base;
+    L->off_wt = L->off_ht + 2 * L->ht_part;
+    L->off_g = L->off_wt + 2 * L->wt_part;
+    L->off_gt = L->off_g + 2 * L->g_bytes;
+    bwd_end = L->off_gt + 2 * L->gt_part;
+  } else {
+    // A small backward step (dH of one strip: few 256 x 256 tiles, a launch of a few waves) runs
+    // overlapped with the next strip's gradient in one launch, which needs a second gradient
+    // strip; a large one fills the GPU by itself and keeps the single strip.
+    const int64_t dh_tiles = ((N + 255) / 256) * ((d + 255) / 256);
+    L->overlap_bwd = (dt == LCE_BF16) && dh_tiles <= kOverlapMaxTiles;
+    L->off_g = base;
+    bwd_end = L->off_g + (L->overlap_bwd ? 2 : 1) * L->g_bytes;
+  }
   L->total = std::max(fwd_end, bwd_end);
   return true;
 }
@@ -143,7 +175,7 @@ cudaError_t traced(int kid, cudaStream_t stream, F&& launch) {
 }
 
 cudaError_t strip_gemm(const StripArgs& a, lce_dtype_t dt, cudaStream_t stream, int num_sms) {
-  if (dt == LCE_BF16)  // the bf16 backward goes through tc_strip_jobs, never through here
+  if (dt != LCE_F32)  // the tensor-core backward goes through tc_strip_jobs, never through here
     return traced(K_TC_FWD, stream, [&] { return tc_strip_gemm(a, stream, num_sms); });
   static const int kid[4] = {K_SIMT_FWD, K_SIMT_BWD_G, K_SIMT_DH, K_SIMT_DW};
   return traced(kid[a.mode], stream, [&] { return simt_strip_gemm(a, stream); });
@@ -153,7 +185,7 @@ lce_status_t common_checks(const void* H, const void* W, const int64_t* labels, 
                            int64_t d, int64_t V, int64_t strip_V, lce_reduction_t red,
                            lce_dtype_t dt, const void* ws, size_t ws_bytes, Layout* L) {
   if (red != LCE_REDUCTION_MEAN && red != LCE_REDUCTION_SUM) return LCE_ERR_INVALID_ARG;
-  if (dt != LCE_BF16 && dt != LCE_F32) return LCE_ERR_INVALID_ARG;
+  if (dt != LCE_BF16 && dt != LCE_F32 && dt != LCE_F32_TF32X3) return LCE_ERR_INVALID_ARG;
   // H and labels may be null only when there is no token
   if (!W || !ws || (N > 0 && (!H || !labels))) return LCE_ERR_INVALID_ARG;
   if (!aligned16(H) || !aligned16(W) || !aligned16(labels) || !aligned16(ws))
@@ -161,6 +193,38 @@ lce_status_t common_checks(const void* H, const void* W, const int64_t* labels, 
   if (!make_layout(N, d, V, strip_V, dt, L)) return LCE_ERR_UNSUPPORTED_SHAPE;
   if (ws_bytes < L->total) return LCE_ERR_WORKSPACE_TOO_SMALL;
   return LCE_OK;
+}
+
+// LCE_F32_TF32X3: tf32 hi / lo parts of n fp32 values into the workspace at `off` (lo at
+// off + part).
+cudaError_t split(const void* x, size_t n, char* ws, size_t off, size_t part, cudaStream_t stream) {
+  return traced(K_SPLIT, stream, [&] {
+    return launch_split_tf32(static_cast<const float*>(x), reinterpret_cast<float*>(ws + off),
+                             reinterpret_cast<float*>(ws + off + part), n, stream);
+  });
+}
+// The same for x [rows x cols], written transposed with row stride ld_out.
+cudaError_t split_t(const void* x, int64_t rows, int64_t cols, int64_t ld_out, char* ws,
+                    size_t off, size_t part, cudaStream_t stream) {
+  return traced(K_SPLIT, stream, [&] {
+    return launch_split_tf32_t(static_cast<const float*>(x), rows, cols, ld_out,
+                               reinterpret_cast<float*>(ws + off),
+                               reinterpret_cast<float*>(ws + off + part), stream);
+  });
+}
+
+// Operands of one LCE_F32_TF32X3 strip GEMM: the split parts of H and of the current W strip
+// (which holds only this strip's rows), and for the backward the transposed parts and G / G^T.
+void set_x3_operands(StripArgs& a, char* ws, const Layout& L) {
+  a.op = OP_TF32X3;
+  a.H = ws + L.off_h;   a.H2 = ws + L.off_h + L.h_part;
+  a.W = ws + L.off_w;   a.W2 = ws + L.off_w + L.w_part;
+  a.w_strip_local = 1;
+  a.HT = ws + L.off_ht; a.HT2 = ws + L.off_ht + L.ht_part;
+  a.WT = ws + L.off_wt; a.WT2 = ws + L.off_wt + L.wt_part;
+  a.G = ws + L.off_g;   a.G2 = ws + L.off_g + L.g_bytes;
+  a.GT = ws + L.off_gt; a.GT2 = ws + L.off_gt + L.gt_part;
+  a.ldt = L.ldt;
 }
 
 }  // namespace
@@ -210,12 +274,16 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels, in
   // covers.  When the partials of the whole vocabulary fit in the workspace sized for strip_V (the
   // backward's gradient strip is larger whenever strip_V >= V/64), one persistent launch covers
   // every strip; otherwise there is one launch per strip.  Either way the workspace is the same.
+  // LCE_F32_TF32X3 splits W one strip at a time, so it keeps one launch per strip.
+  const bool x3 = (dtype == LCE_F32_TF32X3);
   const int64_t tiles_all = (V + L.bn - 1) / L.bn;
   const bool one_launch =
-      L.off_part + static_cast<size_t>(tiles_all) * static_cast<size_t>(N) * sizeof(float2) <=
-      L.total;
+      !x3 && L.off_part + static_cast<size_t>(tiles_all) * static_cast<size_t>(N) * sizeof(float2) <=
+                 L.total;
   const int64_t fwd_step = one_launch ? V : strip_V;
   if (N > 0) {
+    if (x3 && split(H, static_cast<size_t>(N) * d, ws, L.off_h, L.h_part, stream) != cudaSuccess)
+      return LCE_ERR_CUDA;
     for (int64_t col0 = 0, s = 0; col0 < V; col0 += fwd_step, ++s) {
       StripArgs a{};
       a.mode = MODE_FWD_LSE;
@@ -225,6 +293,13 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels, in
       a.part = part; a.tgt = tgt;
       a.labels = labels; a.ignore_index = ignore_index;
       a.err = err; a.first_strip = (s == 0);
+      if (x3) {
+        const float* w_strip = static_cast<const float*>(W) + static_cast<size_t>(col0) * d;
+        if (split(w_strip, static_cast<size_t>(a.strip_cols) * d, ws, L.off_w, L.w_part,
+                  stream) != cudaSuccess)
+          return LCE_ERR_CUDA;
+        set_x3_operands(a, ws, L);
+      }
       if (strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;
       const int tiles = (a.strip_cols + L.bn - 1) / L.bn;
       if (traced(K_COMBINE, stream, [&] {
@@ -288,10 +363,32 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, c
     return a;
   };
   const int64_t S = (V + strip_V - 1) / strip_V;
+  auto run = [&](StripArgs* jobs, int nj) {
+    return traced(K_TC_BWD, stream, [&] { return tc_strip_jobs(jobs, nj, stream, num_sms); });
+  };
+  if (dtype == LCE_F32_TF32X3) {
+    // H split once, plain and transposed.  Per strip: the W strip split, plain and transposed;
+    // one launch for its gradient (G and G^T, hi and lo parts); one launch for dH and dW from it
+    // (dH's tiles first; dH accumulates strip after strip in order).
+    if (split(H, static_cast<size_t>(N) * d, ws, L.off_h, L.h_part, stream) != cudaSuccess ||
+        split_t(H, N, d, L.ldt, ws, L.off_ht, L.ht_part, stream) != cudaSuccess)
+      return LCE_ERR_CUDA;
+    for (int64_t s = 0; s < S; ++s) {
+      StripArgs grad = strip_job(s, MODE_BWD_G, nullptr);
+      StripArgs jobs[2] = {strip_job(s, MODE_DH, nullptr), strip_job(s, MODE_DW, nullptr)};
+      set_x3_operands(grad, ws, L);
+      for (StripArgs& j : jobs) set_x3_operands(j, ws, L);
+      const float* w_strip = static_cast<const float*>(W) + static_cast<size_t>(s * strip_V) * d;
+      if (split(w_strip, static_cast<size_t>(grad.strip_cols) * d, ws, L.off_w, L.w_part,
+                stream) != cudaSuccess ||
+          split_t(w_strip, grad.strip_cols, d, L.ldg, ws, L.off_wt, L.wt_part, stream) !=
+              cudaSuccess)
+        return LCE_ERR_CUDA;
+      if (run(&grad, 1) != cudaSuccess || run(jobs, 2) != cudaSuccess) return LCE_ERR_CUDA;
+    }
+    return LCE_OK;
+  }
   if (dtype == LCE_BF16) {
-    auto run = [&](StripArgs* jobs, int nj) {
-      return traced(K_TC_BWD, stream, [&] { return tc_strip_jobs(jobs, nj, stream, num_sms); });
-    };
     if (L.overlap_bwd) {
       // Step s computes dH and dW of strip s-1 (from gradient buffer (s-1) % 2, the longer
       // reductions first) together with the gradient strip s (into buffer s % 2): one persistent
@@ -397,8 +494,9 @@ int32_t lce_trace_end(void) {
 }
 
 const char* lce_kernel_name(int32_t id) {
-  static const char* names[K_NUM] = {"tc_fwd_lse", "tc_bwd", "simt_fwd_lse", "simt_bwd_grad",
-                                     "simt_dh", "simt_dw", "combine", "finalize"};
+  static const char* names[K_NUM] = {"tc_fwd_lse",    "tc_bwd",  "simt_fwd_lse",
+                                     "simt_bwd_grad", "simt_dh", "simt_dw",
+                                     "combine",       "finalize", "split_tf32"};
   return (id >= 0 && id < K_NUM) ? names[id] : nullptr;
 }
 

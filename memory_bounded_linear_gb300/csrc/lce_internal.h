@@ -26,11 +26,17 @@ enum Mode : int {
 
 // Kernel ids reported by the launch tracer.
 // K_TC_BWD is one backward step: dH and dW of one strip together with the gradient of the next.
+// K_SPLIT is the tf32 hi / lo split of an fp32 operand (plain or transposed).
 enum KernelId : int {
   K_TC_FWD = 0, K_TC_BWD = 1,
   K_SIMT_FWD = 2, K_SIMT_BWD_G = 3, K_SIMT_DH = 4, K_SIMT_DW = 5,
-  K_COMBINE = 6, K_FINALIZE = 7, K_NUM = 8
+  K_COMBINE = 6, K_FINALIZE = 7, K_SPLIT = 8, K_NUM = 9
 };
+
+// Operand formats of the tensor-core engine.  OP_BF16: bf16 operands.  OP_TF32X3: fp32 operands
+// held as tf32 parts x = hi + lo; every product is hi*hi' + hi*lo' + lo*hi'.
+constexpr int OP_BF16 = 0;
+constexpr int OP_TF32X3 = 1;
 
 // Arguments of one strip-GEMM launch (both the tensor-core and the fp32 CUDA-core engines).
 // GEMM view: C[M x Ncols] = A[M x K] * B[Ncols x K]^T.
@@ -52,6 +58,20 @@ struct StripArgs {
   float* C; int64_t ldc; int accumulate; int c_rows; int c_cols;
   unsigned* err;
   int first_strip;
+  // Operand format (OP_*).  For OP_TF32X3, H, W and G point at the hi parts and H2, W2, G2 at
+  // the lo parts.
+  int op;
+  const void* H2; const void* W2; void* G2;
+  // W (and W2) hold only this strip's rows (row 0 = vocabulary column col0), not all V rows.
+  int w_strip_local;
+  // OP_TF32X3 only.  The tf32 MMAs read every operand K-major, so the contractions over the
+  // vocabulary (dH) and over the tokens (dW) take transposed hi / lo copies:
+  //   WT, WT2 [d x ldg]    this strip's rows of W, transposed (dH's B operand)
+  //   HT, HT2 [d x ldt]    H transposed (dW's B operand)
+  //   GT, GT2 [ldg x ldt]  the gradient strip transposed, written by the gradient epilogue
+  //                        beside G (dW's A operand)
+  const void* WT; const void* WT2; const void* HT; const void* HT2; void* GT; void* GT2;
+  int64_t ldt;  // row stride (elements) of HT and GT: N rounded up to a multiple of 32
 };
 
 // Records a human-readable description of the last failure on the calling thread (reported by
@@ -68,13 +88,18 @@ extern int g_tile_config;
 // Test hook: when set, the next tensor-core launch withholds its first k-block (then it clears).
 extern int g_inject_stall;
 
-// Tensor-core (tcgen05) engine, bf16 operands: lce_tc.cu
+// Tensor-core (tcgen05) engine, bf16 or tf32-split fp32 operands: lce_tc.cu
 cudaError_t tc_strip_gemm(const StripArgs& a, cudaStream_t stream, int num_sms);
 // Up to three strip GEMMs in one persistent launch, their tiles scheduled together in order.
 cudaError_t tc_strip_jobs(const StripArgs* jobs, int njobs, cudaStream_t stream, int num_sms);
 // CUDA-core engine, fp32 operands (exact FFMA): lce_simt.cu
 cudaError_t simt_strip_gemm(const StripArgs& a, cudaStream_t stream);
-// Reductions: lce_reduce.cu
+// Reductions and operand splits: lce_reduce.cu
+// x[0..n) -> hi = nearest tf32 of x, lo = nearest tf32 of (x - hi), both in fp32 containers.
+cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, size_t n, cudaStream_t stream);
+// The same split of x [rows x cols] (row-major), written transposed: hi / lo [cols x ld_out].
+cudaError_t launch_split_tf32_t(const float* x, int64_t rows, int64_t cols, int64_t ld_out,
+                                float* hi, float* lo, cudaStream_t stream);
 cudaError_t launch_combine(const float2* part, int tiles, int64_t N, float2* run, int first,
                            cudaStream_t stream);
 cudaError_t launch_finalize(const float2* run, const float* tgt, const int64_t* labels,

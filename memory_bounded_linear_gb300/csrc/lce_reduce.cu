@@ -1,4 +1,4 @@
-// Per-token state reductions of the forward pass.
+// Per-token state reductions of the forward pass, and the tf32 operand splits.
 //
 // combine:  folds the per-(tile, row) (max, sum-exp) partials of one vocabulary strip, in tile
 //           order, into the running per-token state (m, s):
@@ -9,14 +9,20 @@
 // finalize: lse_i = m_i + log s_i for every row; per-token loss lse_i - t_i on valid rows; the
 //           sum over rows in a fixed order in fp64 (one block, fixed per-thread strides and a
 //           fixed tree), n_valid, and the label-range check.
+// split:    fp32 x -> tf32 parts hi = rna(x), lo = rna(x - hi) for the three-product tensor-core
+//           path (x = hi + lo + r with |r| about 2^-22 |x|); plain, or transposed through 32 x 32
+//           shared-memory tiles for the operands the tf32 MMAs need K-major.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "lce_internal.h"
+#include "ptx.cuh"
 
 namespace lce {
 namespace {
+
+using ptx::round_tf32;
 
 __device__ __forceinline__ float2 fold(float2 a, float2 b) {
   const float M = fmaxf(a.x, b.x);
@@ -99,7 +105,81 @@ __global__ void __launch_bounds__(FIN_THREADS)
   }
 }
 
+// Elementwise split, four values per thread, grid-stride.
+__global__ void split_tf32_kernel(const float4* __restrict__ x, float4* __restrict__ hi,
+                                  float4* __restrict__ lo, size_t n4) {
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 v = x[i];
+    float4 h, l;
+    h.x = round_tf32(v.x); l.x = round_tf32(v.x - h.x);
+    h.y = round_tf32(v.y); l.y = round_tf32(v.y - h.y);
+    h.z = round_tf32(v.z); l.z = round_tf32(v.z - h.z);
+    h.w = round_tf32(v.w); l.w = round_tf32(v.w - h.w);
+    hi[i] = h;
+    lo[i] = l;
+  }
+}
+
+// Transposing split: x [rows x cols] -> hi / lo [cols x ld_out], one 32 x 32 tile at a time
+// (grid-stride over tiles); the tile row is padded by one word against bank conflicts, so both
+// the reads of x and the writes of hi / lo are coalesced.
+constexpr int TT = 32;
+
+__global__ void __launch_bounds__(TT * 8)
+    split_tf32_t_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_out,
+                        float* __restrict__ hi, float* __restrict__ lo) {
+  __shared__ float t[TT][TT + 1];
+  const int64_t tiles_c = (cols + TT - 1) / TT;
+  const int64_t tiles = tiles_c * ((rows + TT - 1) / TT);
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int64_t r0 = (tile / tiles_c) * TT, c0 = (tile % tiles_c) * TT;
+    for (int i = threadIdx.y; i < TT; i += 8) {
+      const int64_t r = r0 + i, c = c0 + threadIdx.x;
+      t[i][threadIdx.x] = (r < rows && c < cols) ? x[r * cols + c] : 0.f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < TT; i += 8) {
+      const int64_t c = c0 + i, r = r0 + threadIdx.x;
+      if (c < cols && r < rows) {
+        const float v = t[threadIdx.x][i];
+        const float h = round_tf32(v);
+        hi[c * ld_out + r] = h;
+        lo[c * ld_out + r] = round_tf32(v - h);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Grid-stride kernels run at most a few waves of blocks over the 152 SMs.
+constexpr int64_t kSplitMaxBlocks = 152 * 16;
+
 }  // namespace
+
+cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, size_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  if (n % 4 != 0) return cudaErrorInvalidValue;  // whole rows of d % 8 == 0 elements
+  const size_t n4 = n / 4;
+  const int threads = 256;
+  const int64_t need = static_cast<int64_t>((n4 + threads - 1) / threads);
+  const int64_t blocks = need < kSplitMaxBlocks ? need : kSplitMaxBlocks;
+  split_tf32_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      reinterpret_cast<const float4*>(x), reinterpret_cast<float4*>(hi),
+      reinterpret_cast<float4*>(lo), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_tf32_t(const float* x, int64_t rows, int64_t cols, int64_t ld_out,
+                                float* hi, float* lo, cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (ld_out < rows) return cudaErrorInvalidValue;
+  const int64_t tiles = ((rows + TT - 1) / TT) * ((cols + TT - 1) / TT);
+  const int64_t blocks = tiles < kSplitMaxBlocks ? tiles : kSplitMaxBlocks;
+  split_tf32_t_kernel<<<static_cast<unsigned>(blocks), dim3(TT, 8), 0, stream>>>(x, rows, cols,
+                                                                                ld_out, hi, lo);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const float2* part, int tiles, int64_t N, float2* run, int first,
                            cudaStream_t stream) {

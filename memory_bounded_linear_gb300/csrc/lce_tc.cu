@@ -1,9 +1,11 @@
-// Tensor-core strip GEMM engine for bf16 operands on sm_103a (tcgen05 + TMEM + TMA).
+// Tensor-core strip GEMM engine on sm_103a (tcgen05 + TMEM + TMA), for bf16 operands and for
+// fp32 operands split into tf32 hi / lo parts (three tf32 products per fp32 product).
 //
 // One persistent, warp-specialised kernel.  A launch carries up to three GEMM jobs, each with its
 // own epilogue mode, operands and output; its tiles are scheduled together:
-//   warp 0      TMA producer: streams A and B k-blocks (64 bf16 = one 128-byte swizzle span)
-//               into a shared-memory ring; it also hands out the tiles (dynamic scheduler);
+//   warp 0      TMA producer: streams A and B k-blocks (one 128-byte swizzle span of K: 64 bf16
+//               or 32 fp32 per part) into a shared-memory ring; it also hands out the tiles
+//               (dynamic scheduler);
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and one elected
 //               lane issues tcgen05.mma into the accumulator of the tile;
 //   warps 2..5  epilogue: each thread owns one accumulator row (TMEM lane) and reads its 256
@@ -15,6 +17,9 @@
 //   FWD_LSE, BWD_G  A = H   [N x d] K-major    B = W strip [w x d] K-major
 //   DH              A = G_s [N x w] K-major    B = W strip [w x d] MN-major (d contiguous)
 //   DW              A = G_s^T      MN-major    B = H [N x d]       MN-major
+// For tf32 parts every operand is K-major: dH's B is the transposed strip W_s^T [d x w], dW's A
+// the transposed gradient G_s^T [w x N] (written by the gradient epilogue beside G_s) and its B
+// the transposed H^T [d x N].
 // TMA zero-fills every box element outside the tensor, so ragged M, N and K edges contribute 0
 // to the products; the epilogues mask the columns beyond the strip / vocabulary, and TMA stores
 // clip the output boxes at the edges of their tensors.
@@ -40,8 +45,9 @@ namespace {
 
 constexpr int BM = 128;     // accumulator rows held by one CTA (TMEM lanes)
 constexpr int BN = TC_BN;  // 256 columns per tile
-constexpr int BK = 64;     // one 128-byte swizzle span of bf16
-constexpr int MN_BOX_BYTES = 64 * BK * 2;   // one 64(MN) x 64(K) box of an MN-major operand
+// bf16 MN-major operands: 64(MN) x 64(K) boxes of 8 KB
+constexpr int MN_BOX_ELEMS = 64;
+constexpr int MN_BOX_BYTES = 64 * 64 * 2;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int MAX_STAGES = 6;
@@ -62,19 +68,34 @@ constexpr int MAX_JOBS = 3;
 
 // Tile geometry.  Single: one CTA computes a 128 x 256 tile and holds all of B.  Pair: the two
 // CTAs of a cluster compute a 256 x 256 tile with cta_group::2 MMAs; each holds its 128 rows of
-// A and half (128 columns) of B, so a stage is 32 KB and six stages fit.
-template <bool PAIR>
+// A and half (128 columns) of B.
+// Operand formats.  OP_BF16: one bf16 part per operand, kind::f16 MMAs (K = 16); a bf16 stage
+// is 32 KB in a pair, six stages.  OP_TF32X3: two tf32 parts (hi, lo) per operand, kind::tf32
+// MMAs (K = 8), three MMAs per k-slice (hi*hi' + hi*lo' + lo*hi') into one fp32 accumulator; a
+// stage holds both parts, so there are half as many.  A stage always covers one 128-byte
+// swizzle span of K per row and part, and four MMA k-slices.
+template <bool PAIR, int OP>
 struct Cfg {
+  static constexpr bool X3 = (OP == OP_TF32X3);
+  static constexpr int ELEM = X3 ? 4 : 2;
+  static constexpr int BK = 128 / ELEM;    // K elements per stage
+  static constexpr int KI = X3 ? 8 : 16;   // K of one MMA instruction
+  static constexpr int PARTS = X3 ? 2 : 1;
   static constexpr int TILE_M = PAIR ? 2 * BM : BM;
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // tile columns whose B rows this CTA loads
-  static constexpr int STAGES = PAIR ? 6 : 4;
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = B_ROWS * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int A_BYTES = BM * 128;           // one part of the A block
+  static constexpr int B_BYTES = B_ROWS * 128;       // one part of the B block
+  static constexpr int PART_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGE_BYTES = PARTS * PART_BYTES;
+  static constexpr int STAGES = (PAIR ? 6 : 4) / PARTS;  // 192 KB of stages either way
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + CTL_BYTES;
-  static constexpr int RASTER_GROUP = PAIR ? LCE_PAIR_RASTER_GROUP : 16;  // row tiles per group
   static_assert(STAGES <= MAX_STAGES, "control block sized for MAX_STAGES");
+  static_assert(BK / KI == 4, "four MMA k-slices per stage");
 };
+
+// Row tiles per rasterisation group, by tile variant.
+template <bool PAIR>
+constexpr int RASTER_GROUP = PAIR ? LCE_PAIR_RASTER_GROUP : 16;
 
 // Tiles handed out by the dynamic scheduler wait in a small ring until every role has read them.
 constexpr int TQ = 4;
@@ -121,11 +142,13 @@ struct KParams {
   int inject_stall;  // test hook (lce_test_inject_stall): withhold the first k-block
 };
 
-// Per job: A and B operand maps and the map of the epilogue's TMA stores (G strip or C).
+// Per job: A and B operand maps, one per operand part ([0] only for bf16), and the maps of the
+// epilogue's TMA stores: C in [0]; the bf16 gradient strip in [0]; the tf32 gradient strip's
+// hi and lo parts in [0] and [1], and their transposes in [2] and [3].
 struct TcMaps {
-  CUtensorMap a[MAX_JOBS];
-  CUtensorMap b[MAX_JOBS];
-  CUtensorMap c[MAX_JOBS];
+  CUtensorMap a[MAX_JOBS][2];
+  CUtensorMap b[MAX_JOBS][2];
+  CUtensorMap c[MAX_JOBS][4];
 };
 
 // Bounded wait on an mbarrier phase.  Gives up after WAIT_LIMIT_NS (or at once when another role
@@ -185,7 +208,7 @@ __device__ __forceinline__ TilePos locate(const KParams& p, int t) {
   }
   TilePos r;
   r.job = j;
-  tile_coords(t, p.job[j].tiles_m, p.job[j].tiles_n, Cfg<PAIR>::RASTER_GROUP, r.tm, r.tn);
+  tile_coords(t, p.job[j].tiles_m, p.job[j].tiles_n, RASTER_GROUP<PAIR>, r.tm, r.tn);
   return r;
 }
 
@@ -245,16 +268,30 @@ struct TileQueue {
   }
 };
 
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_base, int k16) {
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_base, int k) {
   // K-major, 128B swizzle: rows of 128 bytes, 8-row swizzle atoms 1024 bytes apart; the k-th
-  // 16-element slice starts 32 bytes further into the row.
-  return ptx::sw128_desc(tile_base + k16 * 32, 16, 1024);
+  // MMA slice (16 bf16 or 8 tf32 elements) starts 32 bytes further into the row.
+  return ptx::sw128_desc(tile_base + k * 32, 16, 1024);
 }
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_base, int k16) {
-  // MN-major, 128B swizzle: each 64-wide MN box holds BK rows (one per k) of 128 bytes; boxes
-  // are MN_BOX_BYTES apart (leading byte offset), groups of 8 k-rows 1024 bytes apart (stride
-  // byte offset); the k-th 16-row slice starts 16 * 128 bytes further.
+  // bf16 MN-major, 128B swizzle: each 64-wide MN box holds 64 rows (one per k) of 128 bytes;
+  // boxes are MN_BOX_BYTES apart (leading byte offset), groups of 8 k-rows 1024 bytes apart
+  // (stride byte offset); the k-th 16-row slice starts 16 * 128 bytes further.
   return ptx::sw128_desc(tile_base + k16 * 16 * 128, MN_BOX_BYTES, 1024);
+}
+
+// Operand majorness per mode.  bf16: dW's A (G, contracted over tokens) and the B operands of dH
+// (W, contracted over the vocabulary) and of dW (H, over tokens) are read MN-major straight from
+// their row-major arrays.  tf32: the kind::tf32 MMAs are given K-major operands only (with an
+// MN-major tf32 operand the accumulator stayed zero on sm_103a), so those operands come from
+// transposed copies.
+template <int MODE, int OP>
+__host__ __device__ constexpr bool a_mn_major() {
+  return MODE == MODE_DW && OP == OP_BF16;
+}
+template <int MODE, int OP>
+__host__ __device__ constexpr bool b_mn_major() {
+  return (MODE == MODE_DH || MODE == MODE_DW) && OP == OP_BF16;
 }
 
 // The kernel is compiled per set of modes it may meet (a bit mask of MODE_*): the forward kernel
@@ -293,22 +330,20 @@ struct Ring {
   uint32_t ph;
 };
 
-// Producer side of one tile: its k-blocks of A and B into the stage ring.  False when a wait
-// gave up.  `withhold_first` is the timeout-path test hook.
-template <int MODE, bool PAIR>
+// Producer side of one tile: its k-blocks of A and B (every operand part) into the stage ring.
+// False when a wait gave up.  `withhold_first` is the timeout-path test hook.
+template <int MODE, bool PAIR, int OP>
 __device__ __forceinline__ bool produce_tile(const Job& jb, const CUtensorMap* mA,
                                              const CUtensorMap* mB, int m0, int n0, uint32_t base,
                                              Ctl* ctl, Ring& r, volatile int* abort_flag,
                                              unsigned* err, uint32_t rank, bool withhold_first) {
-  using Cf = Cfg<PAIR>;
-  constexpr bool A_MN = (MODE == MODE_DW);
-  constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
+  using Cf = Cfg<PAIR, OP>;
+  constexpr bool A_MN = a_mn_major<MODE, OP>();
+  constexpr bool B_MN = b_mn_major<MODE, OP>();
   for (int kb = 0; kb < jb.nkb; ++kb) {
     const uint32_t empty = ptx::smem_addr(&ctl->empty[r.stage]);
     const uint32_t full_local = ptx::smem_addr(&ctl->full[r.stage]);
     if (!wait_bar(empty, r.ph ^ 1u, abort_flag, err)) return false;
-    const uint32_t sa = base + r.stage * Cf::STAGE_BYTES;
-    const uint32_t sb = sa + Cf::A_BYTES;
     const bool withhold = withhold_first && kb == 0 && r.stage == 0 && r.ph == 0;
     if (!withhold) {
       // In a pair every stage's bytes (of both CTAs) are counted on the issuer's barrier.
@@ -318,18 +353,25 @@ __device__ __forceinline__ bool produce_tile(const Job& jb, const CUtensorMap* m
         if (PAIR) ptx::tma_load_2d_pair(dst, m, x, y, full);
         else ptx::tma_load_2d(dst, m, x, y, full);
       };
-      if (A_MN) {
 #pragma unroll
-        for (int c = 0; c < BM / 64; ++c) load(sa + c * MN_BOX_BYTES, mA, m0 + c * 64, kb * BK);
-      } else {
-        load(sa, mA, kb * BK, m0);
-      }
-      if (B_MN) {
-        const int krow = (MODE == MODE_DH ? jb.b_off : 0) + kb * BK;
+      for (int part = 0; part < Cf::PARTS; ++part) {
+        const uint32_t sa = base + r.stage * Cf::STAGE_BYTES + part * Cf::PART_BYTES;
+        const uint32_t sb = sa + Cf::A_BYTES;
+        if (A_MN) {
 #pragma unroll
-        for (int c = 0; c < Cf::B_ROWS / 64; ++c) load(sb + c * MN_BOX_BYTES, mB, n0 + c * 64, krow);
-      } else {
-        load(sb, mB, kb * BK, jb.b_off + n0);
+          for (int c = 0; c < BM / MN_BOX_ELEMS; ++c)
+            load(sa + c * MN_BOX_BYTES, &mA[part], m0 + c * MN_BOX_ELEMS, kb * Cf::BK);
+        } else {
+          load(sa, &mA[part], kb * Cf::BK, m0);
+        }
+        if (B_MN) {
+          const int krow = (MODE == MODE_DH ? jb.b_off : 0) + kb * Cf::BK;
+#pragma unroll
+          for (int c = 0; c < Cf::B_ROWS / MN_BOX_ELEMS; ++c)
+            load(sb + c * MN_BOX_BYTES, &mB[part], n0 + c * MN_BOX_ELEMS, krow);
+        } else {
+          load(sb, &mB[part], kb * Cf::BK, jb.b_off + n0);
+        }
       }
     }  // else (test hook): no bytes, no arrival -- the MMA issuer's wait on this stage runs out
     if (++r.stage == Cf::STAGES) { r.stage = 0; r.ph ^= 1u; }
@@ -337,25 +379,45 @@ __device__ __forceinline__ bool produce_tile(const Job& jb, const CUtensorMap* m
   return true;
 }
 
-// MMA side of one tile: nkb k-blocks of 4 MMAs (K=16 each) into the accumulator at d_tmem.
-template <int MODE, bool PAIR>
+// MMA side of one tile: nkb k-blocks of 4 MMA k-slices (K = 16 bf16, or K = 8 with three tf32
+// products) into the accumulator at d_tmem.
+template <int MODE, bool PAIR, int OP>
 __device__ __forceinline__ bool mma_tile(int nkb, uint32_t d_tmem, uint32_t base, Ctl* ctl, Ring& r,
                                          volatile int* abort_flag, unsigned* err) {
-  using Cf = Cfg<PAIR>;
-  constexpr bool A_MN = (MODE == MODE_DW);
-  constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
-  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(Cf::TILE_M, BN, A_MN, B_MN);
+  using Cf = Cfg<PAIR, OP>;
+  constexpr bool A_MN = a_mn_major<MODE, OP>();
+  constexpr bool B_MN = b_mn_major<MODE, OP>();
+  constexpr uint32_t IDESC = Cf::X3 ? ptx::idesc_tf32_f32(Cf::TILE_M, BN, false, false)
+                                    : ptx::idesc_bf16_f32(Cf::TILE_M, BN, A_MN, B_MN);
+  auto mma = [&](uint64_t ad, uint64_t bd, uint32_t accumulate) {
+    if constexpr (Cf::X3) {
+      if (PAIR) ptx::tc_mma_tf32_pair(d_tmem, ad, bd, IDESC, accumulate);
+      else ptx::tc_mma_tf32(d_tmem, ad, bd, IDESC, accumulate);
+    } else {
+      if (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, IDESC, accumulate);
+      else ptx::tc_mma_f16(d_tmem, ad, bd, IDESC, accumulate);
+    }
+  };
   for (int kb = 0; kb < nkb; ++kb) {
     if (!wait_bar(ptx::smem_addr(&ctl->full[r.stage]), r.ph, abort_flag, err)) return false;
     ptx::tc_fence_after();
-    const uint32_t sa = base + r.stage * Cf::STAGE_BYTES;
-    const uint32_t sb = sa + Cf::A_BYTES;
+    const uint32_t s0 = base + r.stage * Cf::STAGE_BYTES;
 #pragma unroll
-    for (int k = 0; k < BK / 16; ++k) {
-      const uint64_t ad = A_MN ? desc_mnmajor(sa, k) : desc_kmajor(sa, k);
-      const uint64_t bd = B_MN ? desc_mnmajor(sb, k) : desc_kmajor(sb, k);
-      if (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
-      else ptx::tc_mma_f16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+    for (int k = 0; k < Cf::BK / Cf::KI; ++k) {
+      const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+      auto da = [&](int part) {
+        const uint32_t sa = s0 + part * Cf::PART_BYTES;
+        return A_MN ? desc_mnmajor(sa, k) : desc_kmajor(sa, k);
+      };
+      auto db = [&](int part) {
+        const uint32_t sb = s0 + part * Cf::PART_BYTES + Cf::A_BYTES;
+        return B_MN ? desc_mnmajor(sb, k) : desc_kmajor(sb, k);
+      };
+      mma(da(0), db(0), acc);
+      if constexpr (Cf::X3) {
+        mma(da(0), db(1), 1u);  // hi * lo'
+        mma(da(1), db(0), 1u);  // lo * hi'
+      }
     }
     // frees the stage (in both CTAs of a pair) once the MMAs have read it
     if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&ctl->empty[r.stage]), 0x3);
@@ -365,10 +427,10 @@ __device__ __forceinline__ bool mma_tile(int nkb, uint32_t d_tmem, uint32_t base
   return true;
 }
 
-template <int MODES, bool PAIR>
+template <int MODES, bool PAIR, int OP>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_strip_kernel(const __grid_constant__ TcMaps maps, const KParams p) {
-  using Cf = Cfg<PAIR>;
+  using Cf = Cfg<PAIR, OP>;
   constexpr int STAGES = Cf::STAGES;
   constexpr int STAGE_BYTES = Cf::STAGE_BYTES;
 
@@ -422,10 +484,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      for (int j = 0; j < p.njobs; ++j) {
-        ptx::prefetch_tmap(&maps.a[j]);
-        ptx::prefetch_tmap(&maps.b[j]);
-      }
+      for (int j = 0; j < p.njobs; ++j)
+        for (int part = 0; part < Cf::PARTS; ++part) {
+          ptx::prefetch_tmap(&maps.a[j][part]);
+          ptx::prefetch_tmap(&maps.b[j][part]);
+        }
       bool ok = true;
       Ring ring{0, 0u};
       TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u};
@@ -437,9 +500,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int m0 = tp.tm * Cf::TILE_M + static_cast<int>(rank) * BM;       // first A row here
         const int n0 = tp.tn * BN + static_cast<int>(rank) * Cf::B_ROWS * PAIR;  // first B row
         dispatch_mode<MODES>(mode_of<MODES>(jb), [&](auto m) {
-          ok = produce_tile<decltype(m)::value, PAIR>(jb, &maps.a[tp.job], &maps.b[tp.job], m0, n0,
-                                                      base, ctl, ring, abort_flag, p.err, rank,
-                                                      p.inject_stall != 0);
+          ok = produce_tile<decltype(m)::value, PAIR, OP>(jb, maps.a[tp.job], maps.b[tp.job], m0,
+                                                          n0, base, ctl, ring, abort_flag, p.err,
+                                                          rank, p.inject_stall != 0);
         });
       }
       if (!ok) {
@@ -468,7 +531,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         dispatch_mode<MODES>(mode_of<MODES>(jb), [&](auto m) {
-          ok = mma_tile<decltype(m)::value, PAIR>(jb.nkb, d_tmem, base, ctl, ring, abort_flag, p.err);
+          ok = mma_tile<decltype(m)::value, PAIR, OP>(jb.nkb, d_tmem, base, ctl, ring, abort_flag,
+                                                      p.err);
         });
         if (!ok) break;
         // accumulator ready for the epilogue warps (of both CTAs of a pair)
@@ -502,7 +566,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (tile < 0) break;
       const TilePos tp = locate<PAIR>(p, tile);
       const Job& jb = p.job[tp.job];
-      const CUtensorMap* mC = &maps.c[tp.job];
+      const CUtensorMap* mC = maps.c[tp.job];  // C or G in [0]; tf32 gradient parts in [0..3]
       const uint32_t tfull = ptx::smem_addr(&ctl->tfull[acc]);
       const uint32_t tempty_local = ptx::smem_addr(&ctl->tempty[acc]);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
@@ -568,14 +632,88 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (tloc >= 0) p.tgt[row] = t;
           }
         } else {
-          // MODE_BWD_G: G = scale * (exp(Z - lse) - onehot) -> bf16 strip workspace
+          // MODE_BWD_G: G = scale * (exp(Z - lse) - onehot) -> strip workspace
           if (row_ok && !label_ok && y != p.ignore_index && jb.first_strip && tp.tn == 0)
             atomicOr(p.err, ERR_LABEL);
           const float scale = label_ok ? scale_valid : 0.f;
           const float nl = label_ok ? -p.lse[row] * LOG2E : 0.f;
-          // The warp's 32 rows go out as 32 x 64-column boxes through its two staging buffers.
           if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
           ptx::tc_fence_after();
+          if constexpr (OP == OP_TF32X3) {
+            // fp32 gradient as tf32 hi / lo parts.  Per 32 columns the warp writes a 32 x 32 box
+            // of each part into G (rows = its tokens) and then, transposed in shared memory, into
+            // G^T (rows = the columns): lane t stores its value of column j at row j, word t of
+            // the box, in the 128-byte swizzle (16-byte chunk (t/4) ^ (j%8)) -- one word per bank.
+            const uint32_t hbuf = wbuf0, lbuf = wbuf0 + STAGE_BUF_BYTES;
+            const bool rows_live = box_row < p.N;  // the warp holds at least one real token
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+              float g[32];
+              if (c * 32 < ncols) {
+                float v[32];
+                ptx::tmem_load32(tbase + c * 32, v);
+                const int lim = ncols - c * 32;
+                const int jt = tloc - c * 32;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  g[j] = (j < lim) ? scale * exp2f(fmaf(v[j], LOG2E, nl)) : 0.f;
+                  if (j == jt) g[j] -= scale;
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) g[j] = 0.f;
+              }
+              if (!rows_live) continue;
+              if (c > 0) {  // both buffers' previous boxes must have been read
+                if (lane == 0) ptx::bulk_wait_read<0>();
+                __syncwarp();
+              }
+              const uint32_t hrow = hbuf + lane * 128, lrow = lbuf + lane * 128;
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                float h[4], l[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  h[t] = ptx::round_tf32(g[4 * jj + t]);
+                  l[t] = ptx::round_tf32(g[4 * jj + t] - h[t]);
+                }
+                const uint32_t off = (static_cast<uint32_t>(jj) ^ (lane & 7)) << 4;
+                ptx::st_shared_v4(hrow + off, __float_as_uint(h[0]), __float_as_uint(h[1]),
+                                  __float_as_uint(h[2]), __float_as_uint(h[3]));
+                ptx::st_shared_v4(lrow + off, __float_as_uint(l[0]), __float_as_uint(l[1]),
+                                  __float_as_uint(l[2]), __float_as_uint(l[3]));
+              }
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                ptx::tma_store_2d(&mC[0], hbuf, tcol0 + c * 32, box_row);
+                ptx::tma_store_2d(&mC[1], lbuf, tcol0 + c * 32, box_row);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read<0>();
+              }
+              __syncwarp();
+              const uint32_t tw = (static_cast<uint32_t>(lane) & 3u) << 2;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float h = ptx::round_tf32(g[j]);
+                const uint32_t off =
+                    j * 128 + (((static_cast<uint32_t>(lane) >> 2) ^ (j & 7)) << 4) + tw;
+                ptx::st_shared_f32(hbuf + off, h);
+                ptx::st_shared_f32(lbuf + off, ptx::round_tf32(g[j] - h));
+              }
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                ptx::tma_store_2d(&mC[2], hbuf, box_row, tcol0 + c * 32);
+                ptx::tma_store_2d(&mC[3], lbuf, box_row, tcol0 + c * 32);
+                ptx::bulk_commit();
+              }
+            }
+            release();
+            if (lane == 0) ptx::bulk_wait_read<0>();  // both buffers free for the next tile
+            __syncwarp();
+          } else {
+          // The warp's 32 rows go out as 32 x 64-column boxes through its two staging buffers.
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             const uint32_t sbuf = wbuf0 + ((c >> 1) & 1) * STAGE_BUF_BYTES;
@@ -623,6 +761,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           release();
           if (lane == 0) ptx::bulk_wait_read<0>();  // both buffers free for the next tile
           __syncwarp();
+          }
         }
       } else {
         // MODE_DH / MODE_DW: C (+)= accumulator, fp32.  The warp's 32 rows go out as 32 x 32
@@ -726,12 +865,12 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return true;
 }
 
-template <int MODES, bool PAIR>
+template <int MODES, bool PAIR, int OP>
 cudaError_t launch(const TcMaps& maps, const KParams& p, int grid, cudaStream_t stream) {
-  using Cf = Cfg<PAIR>;
+  using Cf = Cfg<PAIR, OP>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_strip_kernel<MODES, PAIR>,
+    cudaError_t e = cudaFuncSetAttribute(tc_strip_kernel<MODES, PAIR, OP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cf::SMEM_BYTES);
     if (e != cudaSuccess) {
@@ -754,55 +893,92 @@ cudaError_t launch(const TcMaps& maps, const KParams& p, int grid, cudaStream_t 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_strip_kernel<MODES, PAIR>, maps, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_strip_kernel<MODES, PAIR, OP>, maps, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess)
-    set_error_detail("launch of the strip GEMM (mode %d%s, %d jobs, grid %d, stream %p): %s",
-                     p.job[0].mode, PAIR ? ", CTA pairs" : "", p.njobs, grid,
+    set_error_detail("launch of the strip GEMM (mode %d%s%s, %d jobs, grid %d, stream %p): %s",
+                     p.job[0].mode, PAIR ? ", CTA pairs" : "", Cf::X3 ? ", tf32 parts" : "",
+                     p.njobs, grid,
                      static_cast<void*>(stream), cudaGetErrorName(e));
   return e;
 }
 
 // Fills job j (maps and tile counts) from one strip GEMM description; false if a map is refused.
-template <bool PAIR>
+// OP_BF16 operands are bf16 arrays; OP_TF32X3 operands are pairs of fp32 arrays (hi, lo), with
+// the transposed copies the K-major tf32 MMAs need for dH and dW.
+template <bool PAIR, int OP>
 bool make_job(const StripArgs& s, TcMaps& maps, Job& jb, int j) {
-  using Cf = Cfg<PAIR>;
+  using Cf = Cfg<PAIR, OP>;
+  constexpr bool X3 = Cf::X3;
+  constexpr int BK = Cf::BK;
+  // the W operand: all V rows, or just this strip's rows starting at row 0
+  const int64_t w_rows = s.w_strip_local ? s.strip_cols : s.V;
+  const int w_row0 = s.w_strip_local ? 0 : s.col0;
+  // one map per operand part: [0] from the hi (or only) array, [1] from the lo array
+  auto parts = [&](CUtensorMap* m, const void* hi, const void* lo, uint64_t inner, uint64_t outer,
+                   uint64_t ld, uint32_t bi, uint32_t bo, char name) {
+    if (!make_map(&m[0], hi, inner, outer, ld, bi, bo, s.mode, name, X3)) return false;
+    if (X3) return make_map(&m[1], lo, inner, outer, ld, bi, bo, s.mode, name, true);
+    m[1] = m[0];
+    return true;
+  };
   int M, Ncols, K;
   bool ok;
   jb = Job{};
   jb.mode = s.mode;
+  for (int c = 0; c < 4; ++c) maps.c[j][c] = CUtensorMap{};
   switch (s.mode) {
     case MODE_FWD_LSE:
     case MODE_BWD_G:
       M = static_cast<int>(s.N);
       Ncols = s.strip_cols;
       K = static_cast<int>(s.d);
-      jb.b_off = s.col0;
-      ok = make_map(&maps.a[j], s.H, s.d, s.N, s.d, BK, BM, s.mode, 'A') &&
-           make_map(&maps.b[j], s.W, s.d, s.V, s.d, BK, Cf::B_ROWS, s.mode, 'B');
-      // gradient strip [N x ldg] bf16, written as 64-column x 32-row boxes
-      if (ok && s.mode == MODE_BWD_G)
-        ok = make_map(&maps.c[j], s.G, s.ldg, s.N, s.ldg, 64, 32, s.mode, 'G');
-      else
-        maps.c[j] = maps.a[j];  // unused by the forward epilogue
+      jb.b_off = w_row0;
+      ok = parts(maps.a[j], s.H, s.H2, s.d, s.N, s.d, BK, BM, 'A') &&
+           parts(maps.b[j], s.W, s.W2, s.d, w_rows, s.d, BK, Cf::B_ROWS, 'B');
+      if (ok && s.mode == MODE_BWD_G) {
+        if (X3) {
+          // gradient strip [N x ldg] hi / lo and its transpose [ldg x ldt] (N tokens per row),
+          // written as 32 x 32 fp32 boxes
+          ok = parts(maps.c[j], s.G, s.G2, s.ldg, s.N, s.ldg, 32, 32, 'G') &&
+               parts(&maps.c[j][2], s.GT, s.GT2, s.N, s.ldg, s.ldt, 32, 32, 'T');
+        } else {
+          // gradient strip [N x ldg] bf16, written as 64-column x 32-row boxes
+          ok = make_map(&maps.c[j][0], s.G, s.ldg, s.N, s.ldg, 64, 32, s.mode, 'G');
+        }
+      }
       break;
     case MODE_DH:
       M = static_cast<int>(s.N);
       Ncols = static_cast<int>(s.d);
       K = s.strip_cols;
-      jb.b_off = s.col0;
-      ok = make_map(&maps.a[j], s.G, s.ldg, s.N, s.ldg, BK, BM, s.mode, 'A') &&
-           make_map(&maps.b[j], s.W, s.d, s.V, s.d, 64, BK, s.mode, 'B') &&
-           make_map(&maps.c[j], s.C, s.d, s.N, s.ldc, 32, 32, s.mode, 'C', true);  // dH fp32
+      if (X3) {
+        // B = W_s^T [d x strip_cols] (row stride ldg): the map stops at the strip's columns, so
+        // the k-block past them reads zeros, not the unwritten padding
+        jb.b_off = 0;
+        ok = parts(maps.a[j], s.G, s.G2, s.ldg, s.N, s.ldg, BK, BM, 'A') &&
+             parts(maps.b[j], s.WT, s.WT2, s.strip_cols, s.d, s.ldg, BK, Cf::B_ROWS, 'B');
+      } else {
+        jb.b_off = w_row0;
+        ok = make_map(&maps.a[j][0], s.G, s.ldg, s.N, s.ldg, BK, BM, s.mode, 'A') &&
+             make_map(&maps.b[j][0], s.W, s.d, w_rows, s.d, MN_BOX_ELEMS, BK, s.mode, 'B');
+      }
+      ok = ok && make_map(&maps.c[j][0], s.C, s.d, s.N, s.ldc, 32, 32, s.mode, 'C', true);
       break;
     case MODE_DW:
       M = s.strip_cols;
       Ncols = static_cast<int>(s.d);
       K = static_cast<int>(s.N);
       jb.b_off = 0;
-      ok = make_map(&maps.a[j], s.G, s.ldg, s.N, s.ldg, 64, BK, s.mode, 'A') &&
-           make_map(&maps.b[j], s.H, s.d, s.N, s.d, 64, BK, s.mode, 'B') &&
-           make_map(&maps.c[j], s.C, s.d, s.strip_cols, s.ldc, 32, 32, s.mode, 'C', true);  // dW_s
+      if (X3) {
+        // A = G_s^T [strip_cols x N], B = H^T [d x N] (row stride ldt): both maps stop at N
+        ok = parts(maps.a[j], s.GT, s.GT2, s.N, s.strip_cols, s.ldt, BK, BM, 'A') &&
+             parts(maps.b[j], s.HT, s.HT2, s.N, s.d, s.ldt, BK, Cf::B_ROWS, 'B');
+      } else {
+        ok = make_map(&maps.a[j][0], s.G, s.ldg, s.N, s.ldg, MN_BOX_ELEMS, BK, s.mode, 'A') &&
+             make_map(&maps.b[j][0], s.H, s.d, s.N, s.d, MN_BOX_ELEMS, BK, s.mode, 'B');
+      }
+      ok = ok && make_map(&maps.c[j][0], s.C, s.d, s.strip_cols, s.ldc, 32, 32, s.mode, 'C', true);
       break;
     default:
       set_error_detail("unknown strip GEMM mode %d", s.mode);
@@ -821,14 +997,14 @@ bool make_job(const StripArgs& s, TcMaps& maps, Job& jb, int j) {
   return true;
 }
 
-template <bool PAIR>
+template <bool PAIR, int OP>
 cudaError_t run(const StripArgs* jobs, int njobs, cudaStream_t stream, int num_sms) {
   TcMaps maps;
   memset(&maps, 0, sizeof(maps));
   KParams p{};
   for (int i = 0; i < njobs; ++i) {
     Job jb;
-    if (!make_job<PAIR>(jobs[i], maps, jb, p.njobs)) return cudaErrorInvalidResourceHandle;
+    if (!make_job<PAIR, OP>(jobs[i], maps, jb, p.njobs)) return cudaErrorInvalidResourceHandle;
     if (jb.num_tiles == 0) continue;  // nothing to compute (e.g. an empty dimension)
     p.job[p.njobs++] = jb;
     p.total_tiles += jb.num_tiles;
@@ -856,8 +1032,8 @@ cudaError_t run(const StripArgs* jobs, int njobs, cudaStream_t stream, int num_s
   const int units = PAIR ? num_sms / 2 : num_sms;
   const int grid = (p.total_tiles < units ? p.total_tiles : units) * (PAIR ? 2 : 1);
   // a launch never mixes the forward with the backward
-  return (p.job[0].mode == MODE_FWD_LSE) ? launch<MODES_FWD, PAIR>(maps, p, grid, stream)
-                                          : launch<MODES_BWD, PAIR>(maps, p, grid, stream);
+  return (p.job[0].mode == MODE_FWD_LSE) ? launch<MODES_FWD, PAIR, OP>(maps, p, grid, stream)
+                                          : launch<MODES_BWD, PAIR, OP>(maps, p, grid, stream);
 }
 
 }  // namespace
@@ -877,7 +1053,14 @@ cudaError_t tc_strip_jobs(const StripArgs* jobs, int njobs, cudaStream_t stream,
   if (g_tile_config == 1) pair = false;
   else if (g_tile_config == 2) pair = true;
   else pair = rows > BM;  // pairs need a second 128-row half to be worth launching
-  return pair ? run<true>(jobs, njobs, stream, num_sms) : run<false>(jobs, njobs, stream, num_sms);
+  // every job of a launch has the first job's operand format
+  for (int i = 1; i < njobs; ++i)
+    if (jobs[i].op != jobs[0].op) return cudaErrorInvalidValue;
+  if (jobs[0].op == OP_TF32X3)
+    return pair ? run<true, OP_TF32X3>(jobs, njobs, stream, num_sms)
+                : run<false, OP_TF32X3>(jobs, njobs, stream, num_sms);
+  return pair ? run<true, OP_BF16>(jobs, njobs, stream, num_sms)
+              : run<false, OP_BF16>(jobs, njobs, stream, num_sms);
 }
 
 cudaError_t tc_strip_gemm(const StripArgs& s, cudaStream_t stream, int num_sms) {

@@ -34,6 +34,7 @@ def test_status_strings_and_kernel_names(lib):
     assert lib.lce_status_string(99) == b"unknown status"
     assert lib.lce_kernel_name(0) == b"tc_fwd_lse"
     assert lib.lce_kernel_name(1) == b"tc_bwd"
+    assert lib.lce_kernel_name(8) == b"split_tf32"
     assert lib.lce_kernel_name(-1) is None and lib.lce_kernel_name(1000) is None
 
 
@@ -55,6 +56,22 @@ def test_workspace_size_formula(lib):
     assert _ws(lib, 100, 64, 300, 4096) == 256 + max(
         ((100 * 8 + 255) // 256 * 256) + ((100 * 4 + 255) // 256 * 256) + ((2 * 100 * 8 + 255) // 256 * 256),
         2 * ((100 * 512 * 2 + 255) // 256 * 256))
+
+
+def test_workspace_size_tf32x3(lib):
+    # three-product tf32 path: header; hi / lo parts of H and of one W strip; then the larger of
+    # the forward region and the backward one (hi / lo parts of H^T, of the W strip transposed,
+    # of the gradient strip and of the gradient strip transposed)
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for N, d, V, s in [(16384, 7168, 200000, 16384), (100, 64, 300, 4096), (33, 8, 1000, 128)]:
+        w = min(s, V)
+        ldg = (w + 255) // 256 * 256
+        ldt = (N + 31) // 32 * 32
+        split = 2 * r(N * d * 4) + 2 * r(w * d * 4)
+        fwd = r(N * 8) + r(N * 4) + r((ldg // 256) * N * 8)
+        bwd = 2 * (r(d * ldt * 4) + r(d * ldg * 4) + r(N * ldg * 4) + r(ldg * ldt * 4))
+        assert _ws(lib, N, d, V, s, 2) == 256 + split + max(fwd, bwd), (N, d, V, s)
+    assert _ws(lib, 100, 64, 300, 4096, 3) == 0  # unknown dtype
 
 
 def test_workspace_is_bounded_by_strip_not_vocab(lib):

@@ -23,23 +23,25 @@ from ._parity import TOL, max_rel, rel_fro
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, strip_V):
+def _run(w, strip_V, f32_mode="exact"):
     H, W, y = make_inputs(w, "cuda", seed=0)
     torch.cuda.synchronize()
     base = torch.cuda.memory_allocated()
     torch.cuda.reset_peak_memory_stats()
-    loss, lse, nv, ws = api.lce_forward(H, W, y, strip_V=strip_V, reduction=w.reduction)
+    loss, lse, nv, ws = api.lce_forward(H, W, y, strip_V=strip_V, reduction=w.reduction,
+                                        f32_mode=f32_mode)
     dH, dW, _ = api.lce_backward(H, W, y, lse, nv, torch.ones((), device="cuda"),
-                                 strip_V=strip_V, reduction=w.reduction, workspace=ws)
+                                 strip_V=strip_V, reduction=w.reduction, workspace=ws,
+                                 f32_mode=f32_mode)
     api.lce_check_error(ws)
     torch.cuda.synchronize()
     _run.extra_peak = torch.cuda.max_memory_allocated() - base
     return H, W, y, loss.item(), lse, int(nv.item()), dH, dW
 
 
-def _check(w, strip_V, full_lse: bool, n_rows=48, n_vocab=24):
-    tl, tg = TOL[w.dtype]
-    H, W, y, loss, lse, nv, dH, dW = _run(w, strip_V)
+def _check(w, strip_V, full_lse: bool, n_rows=48, n_vocab=24, f32_mode="exact"):
+    tl, tg = TOL["tf32x3" if f32_mode == "tf32x3" else w.dtype]
+    H, W, y, loss, lse, nv, dH, dW = _run(w, strip_V, f32_mode)
     peak_after_run = _run.extra_peak  # device memory the forward+backward added
     Hn = H.cpu().double().numpy()
     Wn = W.cpu().double().numpy()
@@ -114,3 +116,10 @@ def test_n32768_d6144_v151552_outliers_sum_strip16384(cuda_lib):
 def test_n16384_d7168_v200000_fp32_strip16384(cuda_lib):
     """The pages' FP32 benchmark shape (Ring-DTP, appendix C), exact fp32 path, fp32 tolerances."""
     _check(WORKLOADS["n16384-d7168-v200000-fp32"], 16384, full_lse=False, n_rows=24, n_vocab=0)
+
+
+def test_n16384_d7168_v200000_fp32_tf32x3_strip16384(cuda_lib):
+    """The same shape on the tensor cores (three tf32 products per fp32 product), fp32
+    tolerances."""
+    _check(WORKLOADS["n16384-d7168-v200000-fp32"], 16384, full_lse=False, n_rows=24, n_vocab=0,
+           f32_mode="tf32x3")

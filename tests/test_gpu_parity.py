@@ -81,6 +81,34 @@ def test_fp32_reduced(cuda_lib, w):
     parity_case(w)
 
 
+@pytest.mark.parametrize("cfg", [1, 2], ids=["single-cta", "cta-pair"])
+@pytest.mark.parametrize("w", [
+    WT.with_sizes(N=300, d=136, V=1000, strip_V=384),      # ragged N, d (K tail), V, strips
+    WT.with_sizes(N=517, d=256, V=2048, strip_V=512, ignore_frac=0.1),
+    WT.with_sizes(N=129, d=64, V=257, strip_V=128, reduction="sum"),
+    WT.with_sizes(N=40, d=8, V=700, strip_V=256),          # N < 128, minimum d
+    WT.with_sizes(N=256, d=1024, V=600, strip_V=1024),     # long K loop, one strip wider than V
+    WT.with_sizes(N=1000, d=96, V=5000, strip_V=128),      # forward strip by strip, many strips
+], ids=["ragged", "ignore10", "tile+1-sum", "N<128-d8", "longK-strip>V", "strip128"])
+def test_tf32x3_each_tile_variant(cuda_lib, tile_config, cfg, w):
+    """fp32 inputs on the tensor cores (three tf32 products of hi / lo parts): the oracle at the
+    fp32 tolerances, with both tile variants, on ragged shapes."""
+    tile_config(cfg)
+    parity_case(w, f32_mode="tf32x3")
+
+
+def test_tf32x3_matches_exact_fp32(cuda_lib):
+    """The two fp32 paths agree with each other far below the bf16 error level."""
+    w = WT.with_sizes(N=700, d=512, V=3000, strip_V=1024)
+    H, W, y = make_inputs(w, "cpu")
+    a = run_gpu(H, W, y, 1024, "mean", f32_mode="exact")
+    b = run_gpu(H, W, y, 1024, "mean", f32_mode="tf32x3")
+    assert abs(a["loss"] - b["loss"]) <= 1e-5 * abs(a["loss"])
+    assert np.max(np.abs(a["lse"] - b["lse"])) <= 1e-4
+    assert rel_fro(b["dH"], a["dH"]) <= 1e-4
+    assert rel_fro(b["dW"], a["dW"]) <= 1e-4
+
+
 @pytest.mark.parametrize("strip", [128, 256, 1024, 4096])
 def test_strip_width_invariance(cuda_lib, strip):
     """Only the order changes with the strip width: every width matches one oracle result."""
@@ -106,13 +134,14 @@ def test_forward_strip_by_strip(cuda_lib, w):
     parity_case(w)
 
 
-@pytest.mark.parametrize("dtype_name", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype_name", ["bf16", "f32", "tf32x3"])
 def test_edge_single_token_and_tiny_vocab(cuda_lib, dtype_name):
     base = W2 if dtype_name == "bf16" else WT
+    mode = "tf32x3" if dtype_name == "tf32x3" else "exact"
     for N, d, V in [(1, 8, 1), (1, 16, 2), (3, 8, 5), (130, 24, 1)]:
         w = base.with_sizes(N=N, d=d, V=V, strip_V=128)
         H, W, y = make_inputs(w, "cpu")
-        g = run_gpu(H, W, y, 128, "mean")
+        g = run_gpu(H, W, y, 128, "mean", f32_mode=mode)
         r = run_oracle(H, W, y, "mean")
         if V == 1:
             assert abs(g["loss"]) < 1e-6
@@ -122,11 +151,13 @@ def test_edge_single_token_and_tiny_vocab(cuda_lib, dtype_name):
             assert_parity(g, r, dtype_name)
 
 
-def test_empty_batch(cuda_lib):
-    w = W2.with_sizes(N=0, d=64, V=300, strip_V=128)
+@pytest.mark.parametrize("dtype_name", ["bf16", "tf32x3"])
+def test_empty_batch(cuda_lib, dtype_name):
+    w = (W2 if dtype_name == "bf16" else WT).with_sizes(N=0, d=64, V=300, strip_V=128)
     H, W, y = make_inputs(w, "cpu")
+    mode = "tf32x3" if dtype_name == "tf32x3" else "exact"
     for red in ("mean", "sum"):
-        g = run_gpu(H, W, y, 128, red)
+        g = run_gpu(H, W, y, 128, red, f32_mode=mode)
         assert g["n_valid"] == 0
         assert np.isnan(g["loss"]) if red == "mean" else g["loss"] == 0.0
         assert g["dH"].shape == (0, 64)
