@@ -466,6 +466,28 @@ def main():
                "overlap": "inputs of step i+1 copied on a second stream during step i"}
         del bufs
 
+    # Delayed weight gradient (lce_backward_parts): the dgrad-only and wgrad-only backward calls
+    # against the fused backward on the same inputs and workspace, CUDA events on the launching
+    # stream, after the timed region.  Each part recomputes its strips' logits.
+    def time_backward(parts, n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        for _ in range(n):
+            api.lce_backward(H, W, y, lse, nv, one, strip_V=S, reduction=w.reduction,
+                             workspace=ws, dH=dH, dW=dW, stream=stream, f32_mode=fm, parts=parts)
+        e1.record(stream)
+        barrier()
+        return max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+
+    n_bwd = max(1, min(5, int(2000.0 / max(time_backward("both", 1), 1e-3))))
+    bwd_ms = {p: time_backward(p, n_bwd) for p in ("both", "dh", "dw")}
+    api.lce_check_error(ws)
+    delayed_wgrad = {"backward_ms": bwd_ms["both"], "dgrad_only_ms": bwd_ms["dh"],
+                     "wgrad_only_ms": bwd_ms["dw"], "iterations": n_bwd,
+                     "critical_path_fraction": bwd_ms["dh"] / bwd_ms["both"]}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, H, W, y)
@@ -491,6 +513,7 @@ def main():
             "roofline": roofline,
             "clocks": clk,
             "e2e": e2e,
+            "delayed_wgrad": delayed_wgrad,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

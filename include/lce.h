@@ -126,6 +126,29 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels,
                           void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Backward, one gradient at a time ("delay wgrad"): "Running 128K-Sequence MoE RL on 32 H100s",
+ * section "Backward Trace: Chunk dgrad and Delay wgrad" -- the data gradient is on the critical
+ * path of the backward pass, the weight gradient is not and can run later (e.g. on another
+ * stream, overlapping the caller's next operation).
+ *   parts = LCE_GRAD_DH: only dH (dW may be NULL, is not touched);
+ *   parts = LCE_GRAD_DW: only dW (dH may be NULL, is not touched);
+ *   parts = LCE_GRAD_DH | LCE_GRAD_DW: exactly lce_backward.
+ * Each call recomputes the strips' logits and gradient itself: the full logit gradient is never
+ * stored, so splitting the two gradients costs one more logit recompute (8 N d V FLOP for both
+ * calls instead of 6 N d V), and takes the dW GEMMs off the critical path (4 N d V FLOP for dH).
+ * The dH and dW written are bitwise identical to those of lce_backward.  Same arguments,
+ * workspace size, errors and ordering as lce_backward; two calls may not share a workspace while
+ * both are in flight.
+ */
+typedef enum { LCE_GRAD_DH = 1, LCE_GRAD_DW = 2 } lce_grad_part_t;
+lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* labels,
+                                const float* lse, const int64_t* n_valid, const float* dloss,
+                                int64_t N, int64_t d, int64_t V, int64_t ignore_index,
+                                int64_t strip_V, lce_reduction_t reduction, lce_dtype_t dtype,
+                                int32_t parts, float* dH, float* dW,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Forward for callers that cannot allocate device memory.  The pages describe no such entry
  * point: it is an addition of this library, with no counterpart in the papers.
  *

@@ -20,6 +20,7 @@ STATUS_NAMES = {
 }
 REDUCTIONS = {"mean": 0, "sum": 1}
 DTYPES = {"bf16": 0, "f32": 1, "tf32x3": 2}
+GRAD_PARTS = {"dh": 1, "dw": 2, "both": 3}
 
 _c_i64 = ctypes.c_int64
 _c_p = ctypes.c_void_p
@@ -31,6 +32,10 @@ _SIGNATURES = {
     "lce_backward": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
                                     _c_i64, _c_i64, ctypes.c_int, ctypes.c_int, _c_p, _c_p, _c_p,
                                     ctypes.c_size_t, _c_p]),
+    "lce_backward_parts": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64,
+                                          _c_i64, _c_i64, _c_i64, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int32, _c_p, _c_p, _c_p, ctypes.c_size_t,
+                                          _c_p]),
     "lce_forward_static_scratch": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64,
                                                   _c_i64, ctypes.c_int, ctypes.c_int, _c_p, _c_p,
                                                   _c_p, _c_p, _c_p]),

@@ -95,8 +95,14 @@ def lce_forward(H, W, labels, *, ignore_index: int = -100, strip_V: int = 8192,
 def lce_backward(H, W, labels, lse, n_valid, dloss, *, ignore_index: int = -100,
                  strip_V: int = 8192, reduction: str = "mean",
                  workspace: Optional[torch.Tensor] = None, dH=None, dW=None,
-                 stream: Optional[torch.cuda.Stream] = None, f32_mode: str = "exact"):
-    """Run the backward entry point.  Returns (dH [N, d] fp32, dW [V, d] fp32, workspace)."""
+                 stream: Optional[torch.cuda.Stream] = None, f32_mode: str = "exact",
+                 parts: str = "both"):
+    """Run the backward entry point.  Returns (dH [N, d] fp32, dW [V, d] fp32, workspace).
+
+    ``parts`` = "dh" or "dw" computes one gradient only (``lce_backward_parts``; the other is
+    returned as None): the data gradient on the critical path now, the weight gradient later."""
+    if parts not in _lib.GRAD_PARTS:
+        raise ValueError(f"parts must be one of {sorted(_lib.GRAD_PARTS)}, got {parts!r}")
     _check_inputs(H, W, labels)
     lib = _lib.load()
     N, d = H.shape
@@ -108,16 +114,29 @@ def lce_backward(H, W, labels, lse, n_valid, dloss, *, ignore_index: int = -100,
     dev = H.device
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    if dH is None:
+    want_dh, want_dw = parts in ("dh", "both"), parts in ("dw", "both")
+    if dH is None and want_dh:
         dH = torch.empty(N, d, dtype=torch.float32, device=dev)
-    if dW is None:
+    if dW is None and want_dw:
         dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+    if not want_dh:
+        dH = None
+    if not want_dw:
+        dW = None
     dloss = dloss.to(device=dev, dtype=torch.float32).contiguous()
     with torch.cuda.device(dev):
-        st = lib.lce_backward(_ptr(H), _ptr(W), _ptr(labels), _ptr(lse), _ptr(n_valid),
-                              _ptr(dloss), N, d, V, ignore_index, strip_V,
-                              _lib.REDUCTIONS[reduction], _lib.DTYPES[dt], _ptr(dH), _ptr(dW),
-                              _ptr(workspace), workspace.numel(), _stream_handle(dev, stream))
+        if parts == "both":
+            st = lib.lce_backward(_ptr(H), _ptr(W), _ptr(labels), _ptr(lse), _ptr(n_valid),
+                                  _ptr(dloss), N, d, V, ignore_index, strip_V,
+                                  _lib.REDUCTIONS[reduction], _lib.DTYPES[dt], _ptr(dH), _ptr(dW),
+                                  _ptr(workspace), workspace.numel(), _stream_handle(dev, stream))
+        else:
+            st = lib.lce_backward_parts(_ptr(H), _ptr(W), _ptr(labels), _ptr(lse), _ptr(n_valid),
+                                        _ptr(dloss), N, d, V, ignore_index, strip_V,
+                                        _lib.REDUCTIONS[reduction], _lib.DTYPES[dt],
+                                        _lib.GRAD_PARTS[parts], _ptr(dH), _ptr(dW),
+                                        _ptr(workspace), workspace.numel(),
+                                        _stream_handle(dev, stream))
     _lib.check(st, "lce_backward")
     return dH, dW, workspace
 

@@ -316,16 +316,21 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels, in
   return LCE_OK;
 }
 
-lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, const float* lse,
-                          const int64_t* n_valid, const float* dloss, int64_t N, int64_t d, int64_t V,
-                          int64_t ignore_index, int64_t strip_V, lce_reduction_t reduction,
-                          lce_dtype_t dtype, float* dH, float* dW, void* workspace,
-                          size_t ws_bytes, void* stream_) {
+lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* labels,
+                                const float* lse, const int64_t* n_valid, const float* dloss,
+                                int64_t N, int64_t d, int64_t V, int64_t ignore_index,
+                                int64_t strip_V, lce_reduction_t reduction, lce_dtype_t dtype,
+                                int32_t parts, float* dH, float* dW, void* workspace,
+                                size_t ws_bytes, void* stream_) {
   Layout L;
   lce_status_t st = common_checks(H, W, labels, N, d, V, strip_V, reduction, dtype, workspace,
                                   ws_bytes, &L);
   if (st != LCE_OK) return st;
-  if (!n_valid || !dloss || !dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
+  if (parts < 1 || parts > (LCE_GRAD_DH | LCE_GRAD_DW)) return LCE_ERR_INVALID_ARG;
+  const bool want_dh = (parts & LCE_GRAD_DH) != 0;
+  const bool want_dw = (parts & LCE_GRAD_DW) != 0;
+  if (!n_valid || !dloss || (want_dw && !dW) || (N > 0 && (!lse || (want_dh && !dH))))
+    return LCE_ERR_INVALID_ARG;
   if (!aligned16(lse) || !aligned16(dH) || !aligned16(dW)) return LCE_ERR_INVALID_ARG;
   int num_sms = 0;
   if ((st = check_device(&num_sms)) != LCE_OK) return st;
@@ -338,8 +343,9 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, c
   if (note(cudaMemsetAsync(ws, 0, WS_HEADER_BYTES, stream)) != cudaSuccess) return LCE_ERR_CUDA;
   if (N == 0) {
     // no token: every logit-gradient row is absent, so dW = 0 (dH has no rows)
-    if (note(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * d * sizeof(float), stream)) !=
-        cudaSuccess)
+    if (want_dw &&
+        note(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * d * sizeof(float), stream)) !=
+            cudaSuccess)
       return LCE_ERR_CUDA;
     return LCE_OK;
   }
@@ -367,24 +373,27 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, c
     return traced(K_TC_BWD, stream, [&] { return tc_strip_jobs(jobs, nj, stream, num_sms); });
   };
   if (dtype == LCE_F32_TF32X3) {
-    // H split once, plain and transposed.  Per strip: the W strip split, plain and transposed;
-    // one launch for its gradient (G and G^T, hi and lo parts); one launch for dH and dW from it
-    // (dH's tiles first; dH accumulates strip after strip in order).
+    // H split once, plain (and transposed for dW).  Per strip: the W strip split, plain (and
+    // transposed for dH); one launch for its gradient (G and G^T, hi and lo parts); one launch
+    // for dH and dW from it (dH's tiles first; dH accumulates strip after strip in order).
     if (split(H, static_cast<size_t>(N) * d, ws, L.off_h, L.h_part, stream) != cudaSuccess ||
-        split_t(H, N, d, L.ldt, ws, L.off_ht, L.ht_part, stream) != cudaSuccess)
+        (want_dw && split_t(H, N, d, L.ldt, ws, L.off_ht, L.ht_part, stream) != cudaSuccess))
       return LCE_ERR_CUDA;
     for (int64_t s = 0; s < S; ++s) {
       StripArgs grad = strip_job(s, MODE_BWD_G, nullptr);
-      StripArgs jobs[2] = {strip_job(s, MODE_DH, nullptr), strip_job(s, MODE_DW, nullptr)};
       set_x3_operands(grad, ws, L);
-      for (StripArgs& j : jobs) set_x3_operands(j, ws, L);
+      StripArgs jobs[2];
+      int nj = 0;
+      if (want_dh) jobs[nj++] = strip_job(s, MODE_DH, nullptr);
+      if (want_dw) jobs[nj++] = strip_job(s, MODE_DW, nullptr);
+      for (int j = 0; j < nj; ++j) set_x3_operands(jobs[j], ws, L);
       const float* w_strip = static_cast<const float*>(W) + static_cast<size_t>(s * strip_V) * d;
       if (split(w_strip, static_cast<size_t>(grad.strip_cols) * d, ws, L.off_w, L.w_part,
                 stream) != cudaSuccess ||
-          split_t(w_strip, grad.strip_cols, d, L.ldg, ws, L.off_wt, L.wt_part, stream) !=
-              cudaSuccess)
+          (want_dh && split_t(w_strip, grad.strip_cols, d, L.ldg, ws, L.off_wt, L.wt_part,
+                              stream) != cudaSuccess))
         return LCE_ERR_CUDA;
-      if (run(&grad, 1) != cudaSuccess || run(jobs, 2) != cudaSuccess) return LCE_ERR_CUDA;
+      if (run(&grad, 1) != cudaSuccess || run(jobs, nj) != cudaSuccess) return LCE_ERR_CUDA;
     }
     return LCE_OK;
   }
@@ -397,10 +406,8 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, c
       for (int64_t s = 0; s <= S; ++s) {
         StripArgs jobs[3];
         int nj = 0;
-        if (s >= 1) {
-          jobs[nj++] = strip_job(s - 1, MODE_DH, gbuf[(s - 1) & 1]);
-          jobs[nj++] = strip_job(s - 1, MODE_DW, gbuf[(s - 1) & 1]);
-        }
+        if (s >= 1 && want_dh) jobs[nj++] = strip_job(s - 1, MODE_DH, gbuf[(s - 1) & 1]);
+        if (s >= 1 && want_dw) jobs[nj++] = strip_job(s - 1, MODE_DW, gbuf[(s - 1) & 1]);
         if (s < S) jobs[nj++] = strip_job(s, MODE_BWD_G, gbuf[s & 1]);
         if (run(jobs, nj) != cudaSuccess) return LCE_ERR_CUDA;
       }
@@ -408,6 +415,7 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, c
       // Per strip: its gradient, then dH and dW from it -- three launches, one gradient strip.
       for (int64_t s = 0; s < S; ++s)
         for (int mode : {MODE_BWD_G, MODE_DH, MODE_DW}) {
+          if ((mode == MODE_DH && !want_dh) || (mode == MODE_DW && !want_dw)) continue;
           StripArgs job = strip_job(s, mode, G);
           if (run(&job, 1) != cudaSuccess) return LCE_ERR_CUDA;
         }
@@ -422,14 +430,24 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, c
     a.mode = MODE_DH;
     a.C = dH; a.ldc = d; a.accumulate = (s > 0); a.c_rows = static_cast<int>(N);
     a.c_cols = static_cast<int>(d);
-    if (strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;
+    if (want_dh && strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;
 
     a.mode = MODE_DW;
     a.C = dW + static_cast<size_t>(col0) * d; a.ldc = d; a.accumulate = 0;
     a.c_rows = a.strip_cols; a.c_cols = static_cast<int>(d);
-    if (strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;
+    if (want_dw && strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;
   }
   return LCE_OK;
+}
+
+lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, const float* lse,
+                          const int64_t* n_valid, const float* dloss, int64_t N, int64_t d, int64_t V,
+                          int64_t ignore_index, int64_t strip_V, lce_reduction_t reduction,
+                          lce_dtype_t dtype, float* dH, float* dW, void* workspace,
+                          size_t ws_bytes, void* stream) {
+  return lce_backward_parts(H, W, labels, lse, n_valid, dloss, N, d, V, ignore_index, strip_V,
+                            reduction, dtype, LCE_GRAD_DH | LCE_GRAD_DW, dH, dW, workspace,
+                            ws_bytes, stream);
 }
 
 lce_status_t lce_check_error(const void* workspace, void* stream_) {

@@ -140,6 +140,24 @@ def test_backward_validation(lib):
     assert bwd(wsb=16) == 3
 
 
+def test_backward_parts_validation(lib):
+    """The one-gradient backward checks its part mask and needs only the requested output."""
+    b = _Buf()
+    p = b.addr
+
+    def bwd(parts, dH=p, dW=p, dl=p, wsb=1 << 20, N=16):
+        return lib.lce_backward_parts(p, p, p, p, p, dl, N, 64, 300, -100, 128, 0, 0, parts,
+                                      dH, dW, p, wsb, None)
+
+    assert bwd(0) == 1 and bwd(4) == 1 and bwd(-1) == 1     # unknown part masks
+    assert bwd(1, dH=None) == 1                              # dH requested, missing
+    assert bwd(2, dW=None) == 1                              # dW requested, missing
+    assert bwd(3, dW=None) == 1
+    assert bwd(1, dH=p + 4) == 1                             # misaligned requested output
+    assert bwd(2, dl=None) == 1
+    assert bwd(1, wsb=16) == 3
+
+
 def test_check_error_and_trace_argument_validation(lib):
     assert lib.lce_check_error(None, None) == 1
     assert lib.lce_trace_begin(None, None, None, 4) == 1

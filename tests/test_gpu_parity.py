@@ -258,3 +258,29 @@ def test_workspace_bound_and_peak_memory(cuda_lib):
     extra = torch.cuda.max_memory_allocated() - base
     assert extra <= sizes[1] + 4 * N * 4 + 4096 + 2 * 1024 * 1024
     assert extra < N * V * 4 / 10
+
+
+@pytest.mark.parametrize("w,mode", [
+    (W2.with_sizes(N=300, d=136, V=1000, strip_V=384), "exact"),     # bf16, overlapped steps
+    (W2.with_sizes(N=4352, d=8192, V=700, strip_V=512), "exact"),    # bf16, 17 x 32 dH tiles: 3 launches/strip
+    (WT.with_sizes(N=100, d=72, V=1000, strip_V=384), "exact"),      # fp32 CUDA cores
+    (WT.with_sizes(N=300, d=136, V=1000, strip_V=384), "tf32x3"),    # fp32 tensor cores
+], ids=["bf16-overlap", "bf16-large-step", "f32", "tf32x3"])
+def test_backward_parts_match_fused_bitwise(cuda_lib, w, mode):
+    """Delayed weight gradient: dH alone and dW alone (lce_backward_parts) are bitwise the dH and
+    dW of the fused backward, and the gradient not asked for is not produced."""
+    H, W, y = make_inputs(w, "cuda")
+    kw = dict(strip_V=w.strip_V, reduction=w.reduction, f32_mode=mode)
+    loss, lse, nv, ws = api.lce_forward(H, W, y, **kw)
+    one = torch.ones((), device="cuda")
+    dH, dW, _ = api.lce_backward(H, W, y, lse, nv, one, workspace=ws, **kw)
+    dH1, no_dW, _ = api.lce_backward(H, W, y, lse, nv, one, workspace=ws, parts="dh", **kw)
+    no_dH, dW2, _ = api.lce_backward(H, W, y, lse, nv, one, workspace=ws, parts="dw", **kw)
+    api.lce_check_error(ws)
+    assert no_dW is None and no_dH is None
+    assert torch.equal(dH, dH1)
+    assert torch.equal(dW, dW2)
+    r = run_oracle(H.cpu(), W.cpu(), y.cpu(), w.reduction)
+    tol = 1e-2 if w.dtype == "bf16" else 1e-4
+    assert rel_fro(dH1.cpu().double().numpy(), r["dH"]) <= tol
+    assert rel_fro(dW2.cpu().double().numpy(), r["dW"]) <= tol
