@@ -80,7 +80,7 @@ void set_error_detail(const char* fmt, ...);
 
 // Tile widths of the two engines (columns of a logit tile).
 constexpr int TC_BN = 256;
-constexpr int SIMT_BN = 64;
+constexpr int SIMT_BN = 128;
 
 // Tile variant of the tensor-core engine: 0 automatic, 1 single-CTA 128x256 tiles, 2 CTA-pair
 // 256x256 tiles (set through lce_set_tile_config).

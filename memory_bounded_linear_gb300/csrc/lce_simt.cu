@@ -1,9 +1,16 @@
-// CUDA-core strip GEMM engine for fp32 operands (exact fp32 FFMA; TF32 tensor cores would not
-// hold fp32 accuracy).  Same four epilogue modes and the same workspace contract as the
-// tensor-core engine, with 64 x 64 output tiles:
-//   FWD_LSE  per-(row, 64-column tile) (max, sum-exp) partial and the target logit
+// CUDA-core strip GEMM engine for fp32 operands with exact fp32 products (FFMA).  Same four
+// epilogue modes and the same workspace contract as the tensor-core engine, with 128 x 128
+// output tiles:
+//   FWD_LSE  per-(row, 128-column tile) (max, sum-exp) partial and the target logit
 //   BWD_G    G = scale (softmax - onehot) into the fp32 strip workspace
 //   DH       dH (+)= G_s W_s           DW   dW_s = G_s^T H
+//
+// A register-tiled SGEMM: 256 threads, each owning an 8 x 8 block of the tile as 2 x 2 sub-blocks
+// of 4 x 4 (rows ty*4 + {0..3} and 64 + ty*4 + {0..3}, columns likewise with tx), k-blocks of 8
+// staged in shared memory as [k][m] and [k][n] rows, so every k step is two float4 reads of A and
+// two of B for 64 FFMAs.  The next k-block is loaded into registers while the current one is
+// multiplied (one barrier per k-block).  Operands are K-major or MN-major per mode; both are read
+// as float4 along their contiguous dimension, with a scalar path at the ragged edges.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -13,15 +20,19 @@
 namespace lce {
 namespace {
 
-constexpr int TM = 64;
-constexpr int TN = SIMT_BN;  // 64
-constexpr int TK = 16;
-constexpr int THREADS = 256;  // 16 x 16 threads, 4 x 4 outputs each
+constexpr int TM = 128;
+constexpr int TN = SIMT_BN;  // 128
+constexpr int TK = 8;
+constexpr int THREADS = 256;  // 16 x 16 threads, 8 x 8 outputs each
+constexpr int PAD = 4;        // keeps rows 16-byte aligned and spreads the transposed stores
+constexpr int RASTER = 8;     // row tiles per rasterisation group
+static_assert(TN == 128, "the epilogues assume 128-column tiles");
 
 struct SParams {
   int M, Ncols, K;
-  int tiles_n;
-  // element (m, k) of A is A[m * a_sm + k * a_sk]; (n, k) of B is B[n * b_sn + k * b_sk]
+  int tiles_m, tiles_n;
+  // element (m, k) of A is A[m * a_sm + k * a_sk]; (n, k) of B is B[n * b_sn + k * b_sk]; one of
+  // the two strides of each operand is 1
   const float* A;
   int64_t a_sm, a_sk;
   const float* B;
@@ -44,73 +55,147 @@ struct SParams {
   int first_strip;
 };
 
-template <int MODE>
-__global__ void __launch_bounds__(THREADS) simt_strip_kernel(const SParams p) {
-  __shared__ float As[TK][TM + 4];
-  __shared__ float Bs[TK][TN + 4];
-  __shared__ float Cs[TM][TN + 1];
+// One thread's share of a TK x 128 operand block: four consecutive elements along the operand's
+// contiguous dimension.  K-major (stride 1 along k): row r = t / 2 of the block, k offset
+// (t % 2) * 4.  MN-major (stride 1 along m): k row t / 32, m offset (t % 32) * 4.
+struct Frag {
+  float v[4];
+};
 
-  const int tm = blockIdx.y, tn = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;
-  const int m0 = tm * TM, n0 = tn * TN;
-
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < p.K; k0 += TK) {
-    for (int i = tid; i < TM * TK; i += THREADS) {
-      // K-major operands walk k fastest, MN-major operands walk m fastest (coalesced either way)
-      int mm, kk;
-      if (p.a_sk == 1) { mm = i / TK; kk = i % TK; } else { mm = i % TM; kk = i / TM; }
-      const int gm = m0 + mm, gk = k0 + kk;
-      As[kk][mm] = (gm < p.M && gk < p.K) ? p.A[gm * p.a_sm + gk * p.a_sk] : 0.f;
-      int nn, kb;
-      if (p.b_sk == 1) { nn = i / TK; kb = i % TK; } else { nn = i % TN; kb = i / TN; }
-      const int gn = n0 + nn, gkb = k0 + kb;
-      Bs[kb][nn] = (gn < p.Ncols && gkb < p.K) ? p.B[gn * p.b_sn + gkb * p.b_sk] : 0.f;
+__device__ __forceinline__ void load_frag(Frag& f, const float* __restrict__ X, int64_t s_mn,
+                                          int64_t s_k, bool k_major, int mn0, int k0, int MN,
+                                          int K, int t) {
+  int mn, k;
+  if (k_major) { mn = mn0 + t / 2; k = k0 + (t % 2) * 4; }
+  else { mn = mn0 + (t % 32) * 4; k = k0 + t / 32; }
+  const float* p = X + static_cast<int64_t>(mn) * s_mn + static_cast<int64_t>(k) * s_k;
+  const bool full = k_major ? (mn < MN && k + 3 < K) : (k < K && mn + 3 < MN);
+  if (full) {
+    const float4 q = *reinterpret_cast<const float4*>(p);  // 16-byte aligned: see simt_strip_gemm
+    f.v[0] = q.x; f.v[1] = q.y; f.v[2] = q.z; f.v[3] = q.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const bool ok = k_major ? (mn < MN && k + i < K) : (k < K && mn + i < MN);
+      f.v[i] = ok ? p[i] : 0.f;  // stride 1 along the contiguous dimension either way
     }
-    __syncthreads();
+  }
+}
+
+__device__ __forceinline__ void store_frag(float (*S)[TM + PAD], const Frag& f, bool k_major,
+                                           int t) {
+  if (k_major) {
+    const int mn = t / 2, k = (t % 2) * 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) S[k + i][mn] = f.v[i];
+  } else {
+    *reinterpret_cast<float4*>(&S[t / 32][(t % 32) * 4]) =
+        make_float4(f.v[0], f.v[1], f.v[2], f.v[3]);
+  }
+}
+
+// Grouped rasterisation: RASTER row tiles sweep the column tiles together (operand reuse in L2).
+__device__ __forceinline__ void tile_of(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int per_group = RASTER * tiles_n;
+  const int g = t / per_group;
+  const int first = g * RASTER;
+  const int gm = min(tiles_m - first, RASTER);
+  const int r = t - g * per_group;
+  tm = first + r % gm;
+  tn = r / gm;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 2) simt_strip_kernel(const SParams p) {
+  __shared__ __align__(16) float As[2][TK][TM + PAD];
+  __shared__ __align__(16) float Bs[2][TK][TN + PAD];
+
+  int tm, tn;
+  tile_of(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
+  const int t = threadIdx.x;
+  const int tx = t & 15, ty = t >> 4;
+  const int m0 = tm * TM, n0 = tn * TN;
+  const bool a_kmaj = (p.a_sk == 1), b_kmaj = (p.b_sk == 1);
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  Frag fa, fb;
+  load_frag(fa, p.A, p.a_sm, p.a_sk, a_kmaj, m0, 0, p.M, p.K, t);
+  load_frag(fb, p.B, p.b_sn, p.b_sk, b_kmaj, n0, 0, p.Ncols, p.K, t);
+  store_frag(As[0], fa, a_kmaj, t);
+  store_frag(Bs[0], fb, b_kmaj, t);
+  __syncthreads();
+  const int nkb = (p.K + TK - 1) / TK;
+  for (int kb = 0; kb < nkb; ++kb) {
+    const int cur = kb & 1;
+    const bool more = kb + 1 < nkb;
+    if (more) {  // next k-block into registers while this one is multiplied
+      load_frag(fa, p.A, p.a_sm, p.a_sk, a_kmaj, m0, (kb + 1) * TK, p.M, p.K, t);
+      load_frag(fb, p.B, p.b_sn, p.b_sk, b_kmaj, n0, (kb + 1) * TK, p.Ncols, p.K, t);
+    }
 #pragma unroll
     for (int kk = 0; kk < TK; ++kk) {
-      float a[4], b[4];
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][kk][64 + tx * 4]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    if (more) {  // the other buffer was last read before the previous barrier
+      store_frag(As[cur ^ 1], fa, a_kmaj, t);
+      store_frag(Bs[cur ^ 1], fb, b_kmaj, t);
     }
     __syncthreads();
   }
 
+  // this thread's rows and columns (tile-local): r(i) = (i / 4) * 64 + ty * 4 + i % 4, same for c
+  auto row_of = [&](int i) { return (i >> 2) * 64 + ty * 4 + (i & 3); };
+  auto col_of = [&](int j) { return (j >> 2) * 64 + tx * 4 + (j & 3); };
+
   if (MODE == MODE_FWD_LSE) {
+    // The 16 threads sharing a row (tx = 0..15) are one half-warp: reduce over them by shuffles.
+    const int ncols = min(TN, p.strip_cols - n0);  // >= 1
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i) {
+      const int row = m0 + row_of(i);
+      float mx = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) Cs[ty * 4 + i][tx * 4 + j] = acc[i][j];
-    __syncthreads();
-    if (tid < TM) {
-      const int row = m0 + tid;
+      for (int j = 0; j < 8; ++j)
+        if (col_of(j) < ncols) mx = fmaxf(mx, acc[i][j]);
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float sm = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (col_of(j) < ncols) sm += expf(acc[i][j] - mx);
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
       if (row < p.M) {
-        const int ncols = min(TN, p.strip_cols - n0);
-        float m = -INFINITY;
-        for (int j = 0; j < ncols; ++j) m = fmaxf(m, Cs[tid][j]);
-        float s = 0.f;
-        for (int j = 0; j < ncols; ++j) s += expf(Cs[tid][j] - m);
-        p.part[static_cast<size_t>(tn) * p.M + row] = make_float2(m, s);
+        if (tx == 0) p.part[static_cast<size_t>(tn) * p.M + row] = make_float2(mx, sm);
         const int64_t y = p.labels[row];
         const int64_t rel = y - static_cast<int64_t>(p.col0 + n0);
-        if (y != p.ignore_index && y >= 0 && y < p.V && rel >= 0 && rel < ncols)
-          p.tgt[row] = Cs[tid][rel];
+        if (y != p.ignore_index && y >= 0 && y < p.V && rel >= 0 && rel < ncols) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (col_of(j) == rel) p.tgt[row] = acc[i][j];
+        }
       }
     }
   } else if (MODE == MODE_BWD_G) {
     const float dl = *p.dloss;
     const float scale_valid = (p.reduction == 0) ? dl / static_cast<float>(*p.n_valid) : dl;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int row = m0 + ty * 4 + i;
+    for (int i = 0; i < 8; ++i) {
+      const int row = m0 + row_of(i);
       if (row >= p.M) continue;
       const int64_t y = p.labels[row];
       const bool ok = (y != p.ignore_index) && (y >= 0) && (y < p.V);
@@ -118,27 +203,38 @@ __global__ void __launch_bounds__(THREADS) simt_strip_kernel(const SParams p) {
         atomicOr(p.err, ERR_LABEL);
       const float l = ok ? p.lse[row] : 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int col = n0 + tx * 4 + j;  // strip-local column, < ldg by construction
-        float g = 0.f;
-        if (ok && col < p.strip_cols) {
-          g = scale_valid * expf(acc[i][j] - l);
-          if (static_cast<int64_t>(p.col0 + col) == y) g -= scale_valid;
+      for (int h = 0; h < 2; ++h) {
+        float g[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int col = n0 + col_of(h * 4 + q);  // strip-local column, < ldg by construction
+          g[q] = 0.f;
+          if (ok && col < p.strip_cols) {
+            g[q] = scale_valid * expf(acc[i][h * 4 + q] - l);
+            if (static_cast<int64_t>(p.col0 + col) == y) g[q] -= scale_valid;
+          }
         }
-        p.G[static_cast<size_t>(row) * p.ldg + col] = g;
+        *reinterpret_cast<float4*>(p.G + static_cast<size_t>(row) * p.ldg + n0 + col_of(h * 4)) =
+            make_float4(g[0], g[1], g[2], g[3]);
       }
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int row = m0 + ty * 4 + i;
+    for (int i = 0; i < 8; ++i) {
+      const int row = m0 + row_of(i);
       if (row >= p.c_rows) continue;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int col = n0 + tx * 4 + j;
-        if (col >= p.c_cols) continue;
-        float* c = p.C + static_cast<size_t>(row) * p.ldc + col;
-        *c = p.accumulate ? *c + acc[i][j] : acc[i][j];
+      for (int h = 0; h < 2; ++h) {
+        const int col = n0 + col_of(h * 4);
+        if (col >= p.c_cols) continue;  // c_cols % 4 == 0: a group is all in or all out
+        float4* c = reinterpret_cast<float4*>(p.C + static_cast<size_t>(row) * p.ldc + col);
+        float4 v = make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2],
+                               acc[i][h * 4 + 3]);
+        if (p.accumulate) {
+          const float4 o = *c;
+          v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+        }
+        *c = v;
       }
     }
   }
@@ -146,6 +242,10 @@ __global__ void __launch_bounds__(THREADS) simt_strip_kernel(const SParams p) {
 
 }  // namespace
 
+// Alignment of the float4 accesses: every operand base is 16-byte aligned (caller pointers, the
+// W strip at col0 * d with d % 8 == 0, workspace offsets), every row stride is a multiple of 4
+// elements (d % 8 == 0, ldg % 128 == 0), and float4 offsets along the contiguous dimension are
+// multiples of 4.
 cudaError_t simt_strip_gemm(const StripArgs& s, cudaStream_t stream) {
   SParams p{};
   const float* H = static_cast<const float*>(s.H);
@@ -172,7 +272,9 @@ cudaError_t simt_strip_gemm(const StripArgs& s, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   if (p.M == 0 || p.Ncols == 0 || p.K == 0) return cudaSuccess;
+  p.tiles_m = (p.M + TM - 1) / TM;
   p.tiles_n = (p.Ncols + TN - 1) / TN;
+  if (static_cast<int64_t>(p.tiles_m) * p.tiles_n > 0x7fffffffLL) return cudaErrorInvalidValue;
   p.strip_cols = s.strip_cols; p.col0 = s.col0;
   p.part = s.part; p.tgt = s.tgt;
   p.labels = s.labels; p.V = s.V; p.ignore_index = s.ignore_index;
@@ -180,7 +282,7 @@ cudaError_t simt_strip_gemm(const StripArgs& s, cudaStream_t stream) {
   p.G = static_cast<float*>(s.G); p.ldg = s.ldg;
   p.C = s.C; p.ldc = s.ldc; p.accumulate = s.accumulate; p.c_rows = s.c_rows; p.c_cols = s.c_cols;
   p.err = s.err; p.first_strip = s.first_strip;
-  const dim3 grid(p.tiles_n, (p.M + TM - 1) / TM);
+  const unsigned grid = static_cast<unsigned>(p.tiles_m * p.tiles_n);
   switch (s.mode) {
     case MODE_FWD_LSE: simt_strip_kernel<MODE_FWD_LSE><<<grid, THREADS, 0, stream>>>(p); break;
     case MODE_BWD_G: simt_strip_kernel<MODE_BWD_G><<<grid, THREADS, 0, stream>>>(p); break;

@@ -50,7 +50,7 @@ def test_workspace_size_formula(lib):
     assert _ws(lib, N, d, V, s) == 256 + g_bytes
     # bf16, small backward step (16 x 8 dH tiles): two gradient strips, consecutive strips overlap
     assert _ws(lib, 4096, 2048, 151936, 8192) == 256 + 2 * 4096 * 8192 * 2
-    # fp32 engine: 64-wide tiles, one fp32 gradient strip
+    # fp32 engine: 128-wide tiles, one fp32 gradient strip
     assert _ws(lib, 256, 256, 4096, 512, 1) == 256 + 256 * 512 * 4
     # strip wider than V: the strip is V wide (padded to the tile width)
     assert _ws(lib, 100, 64, 300, 4096) == 256 + max(
