@@ -6,7 +6,7 @@
 //   DH       dH (+)= G_s W_s           DW   dW_s = G_s^T H
 //
 // A register-tiled SGEMM: 256 threads, each owning an 8 x 8 block of the tile as 2 x 2 sub-blocks
-// of 4 x 4 (rows ty*4 + {0..3} and 64 + ty*4 + {0..3}, columns likewise with tx), k-blocks of 8
+// of 4 x 4 (rows ty*4 + {0..3} and 64 + ty*4 + {0..3}, columns likewise with tx), k-blocks of 16
 // staged in shared memory as [k][m] and [k][n] rows, so every k step is two float4 reads of A and
 // two of B for 64 FFMAs.  The next k-block is loaded into registers while the current one is
 // multiplied (one barrier per k-block).  Operands are K-major or MN-major per mode; both are read
@@ -15,6 +15,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "lce_internal.h"
 
 namespace lce {
@@ -22,11 +24,15 @@ namespace {
 
 constexpr int TM = 128;
 constexpr int TN = SIMT_BN;  // 128
-constexpr int TK = 8;
+constexpr int TK = 16;
 constexpr int THREADS = 256;  // 16 x 16 threads, 8 x 8 outputs each
-constexpr int PAD = 4;        // keeps rows 16-byte aligned and spreads the transposed stores
 constexpr int RASTER = 8;     // row tiles per rasterisation group
 static_assert(TN == 128, "the epilogues assume 128-column tiles");
+// Resident blocks per SM the kernel is compiled for (build-time tunable): 2 caps registers at
+// 128 per thread; 1 leaves the compiler up to 255.
+#ifndef LCE_SIMT_MIN_BLOCKS
+#define LCE_SIMT_MIN_BLOCKS 2
+#endif
 
 struct SParams {
   int M, Ncols, K;
@@ -55,44 +61,72 @@ struct SParams {
   int first_strip;
 };
 
-// One thread's share of a TK x 128 operand block: four consecutive elements along the operand's
-// contiguous dimension.  K-major (stride 1 along k): row r = t / 2 of the block, k offset
-// (t % 2) * 4.  MN-major (stride 1 along m): k row t / 32, m offset (t % 32) * 4.
-struct Frag {
-  float v[4];
-};
+// Shared-memory layout of a staged operand block: [TK][128] floats, element (k, m) at column
+// m ^ swz(k).  The swizzle flips bits 3-4 of m by k / 4, so the transposed scalar stores of a
+// K-major block (8 consecutive m by 4 k-groups per warp) land in 32 distinct banks, while groups
+// of 4 consecutive m stay contiguous for the float4 reads of the multiply.
+__device__ __forceinline__ int swz(int k) { return ((k >> 2) & 3) << 3; }
 
-__device__ __forceinline__ void load_frag(Frag& f, const float* __restrict__ X, int64_t s_mn,
-                                          int64_t s_k, bool k_major, int mn0, int k0, int MN,
-                                          int K, int t) {
-  int mn, k;
-  if (k_major) { mn = mn0 + t / 2; k = k0 + (t % 2) * 4; }
-  else { mn = mn0 + (t % 32) * 4; k = k0 + t / 32; }
-  const float* p = X + static_cast<int64_t>(mn) * s_mn + static_cast<int64_t>(k) * s_k;
-  const bool full = k_major ? (mn < MN && k + 3 < K) : (k < K && mn + 3 < MN);
-  if (full) {
-    const float4 q = *reinterpret_cast<const float4*>(p);  // 16-byte aligned: see simt_strip_gemm
-    f.v[0] = q.x; f.v[1] = q.y; f.v[2] = q.z; f.v[3] = q.w;
-  } else {
+// A thread's two fragments of a TK x 128 operand block, four consecutive elements each along the
+// operand's contiguous dimension.  Fragment f covers u = t + 256 f:
+//   K-major (stride 1 along k):  m = u / 4,  k = (u % 4) * 4       (fragment 1: m + 64)
+//   MN-major (stride 1 along m): k = u / 32, m = (u % 32) * 4      (fragment 1: k + 8)
+// One base pointer per operand (fragment 0 of the current k-block) advances by TK along k.
+template <bool KMAJ>
+struct Operand {
+  const float* base;
+  int64_t step;  // elements between consecutive k-blocks
+  int off1;      // fragment 1 relative to fragment 0 (64 rows, or 8 k-rows)
+  int mn0, k0;   // fragment 0's m and k offsets within the block (tile-relative m added)
+  unsigned ok;   // bit f: fragment f's m range lies inside the operand
+
+  __device__ __forceinline__ void init(const float* X, int64_t s_mn, int64_t s_k, int tile_mn,
+                                       int MN, int t) {
+    mn0 = tile_mn + (KMAJ ? t / 4 : (t % 32) * 4);
+    k0 = KMAJ ? (t % 4) * 4 : t / 32;
+    base = X + static_cast<int64_t>(mn0) * s_mn + static_cast<int64_t>(k0) * s_k;
+    off1 = KMAJ ? static_cast<int>(64 * s_mn) : static_cast<int>(8 * s_k);
+    step = static_cast<int64_t>(TK) * s_k;
+    ok = KMAJ ? ((mn0 < MN ? 1u : 0u) | (mn0 + 64 < MN ? 2u : 0u))
+              : (mn0 + 3 < MN ? 3u : 0u);
+  }
+
+  // k-block kb (base already advanced to it); `kfull`: the whole block lies inside K.  Off the
+  // fast path every element is checked on its own (ragged M, N or K edges).
+  __device__ __forceinline__ void load(int kb, bool kfull, int MN, int K, float (&v)[2][4]) const {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const bool ok = k_major ? (mn < MN && k + i < K) : (k < K && mn + i < MN);
-      f.v[i] = ok ? p[i] : 0.f;  // stride 1 along the contiguous dimension either way
+    for (int f = 0; f < 2; ++f) {
+      const float* p = base + (f ? off1 : 0);
+      if (kfull && ((ok >> f) & 1u)) {
+        const float4 q = *reinterpret_cast<const float4*>(p);  // 16-byte aligned: see simt_strip_gemm
+        v[f][0] = q.x; v[f][1] = q.y; v[f][2] = q.z; v[f][3] = q.w;
+      } else {
+        const int mn = mn0 + ((KMAJ && f) ? 64 : 0);
+        const int k = kb * TK + k0 + ((!KMAJ && f) ? 8 : 0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const bool in = KMAJ ? (mn < MN && k + i < K) : (k < K && mn + i < MN);
+          v[f][i] = in ? p[i] : 0.f;  // stride 1 along the contiguous dimension either way
+        }
+      }
     }
   }
-}
 
-__device__ __forceinline__ void store_frag(float (*S)[TM + PAD], const Frag& f, bool k_major,
-                                           int t) {
-  if (k_major) {
-    const int mn = t / 2, k = (t % 2) * 4;
+  __device__ __forceinline__ void store(float (*S)[TM], const float (&v)[2][4], int t) const {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) S[k + i][mn] = f.v[i];
-  } else {
-    *reinterpret_cast<float4*>(&S[t / 32][(t % 32) * 4]) =
-        make_float4(f.v[0], f.v[1], f.v[2], f.v[3]);
+    for (int f = 0; f < 2; ++f) {
+      if (KMAJ) {
+        const int m = t / 4 + 64 * f, k = (t % 4) * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) S[k + i][m ^ swz(k + i)] = v[f][i];
+      } else {
+        const int k = t / 32 + 8 * f, m = (t % 32) * 4;
+        *reinterpret_cast<float4*>(&S[k][m ^ swz(k)]) =
+            make_float4(v[f][0], v[f][1], v[f][2], v[f][3]);
+      }
+    }
   }
-}
+};
 
 // Grouped rasterisation: RASTER row tiles sweep the column tiles together (operand reuse in L2).
 __device__ __forceinline__ void tile_of(int t, int tiles_m, int tiles_n, int& tm, int& tn) {
@@ -106,16 +140,15 @@ __device__ __forceinline__ void tile_of(int t, int tiles_m, int tiles_n, int& tm
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(THREADS, 2) simt_strip_kernel(const SParams p) {
-  __shared__ __align__(16) float As[2][TK][TM + PAD];
-  __shared__ __align__(16) float Bs[2][TK][TN + PAD];
+__global__ void __launch_bounds__(THREADS, LCE_SIMT_MIN_BLOCKS) simt_strip_kernel(const SParams p) {
+  __shared__ __align__(16) float As[2][TK][TM];
+  __shared__ __align__(16) float Bs[2][TK][TN];
 
   int tm, tn;
   tile_of(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
   const int t = threadIdx.x;
   const int tx = t & 15, ty = t >> 4;
   const int m0 = tm * TM, n0 = tn * TN;
-  const bool a_kmaj = (p.a_sk == 1), b_kmaj = (p.b_sk == 1);
 
   float acc[8][8];
 #pragma unroll
@@ -123,26 +156,36 @@ __global__ void __launch_bounds__(THREADS, 2) simt_strip_kernel(const SParams p)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-  Frag fa, fb;
-  load_frag(fa, p.A, p.a_sm, p.a_sk, a_kmaj, m0, 0, p.M, p.K, t);
-  load_frag(fb, p.B, p.b_sn, p.b_sk, b_kmaj, n0, 0, p.Ncols, p.K, t);
-  store_frag(As[0], fa, a_kmaj, t);
-  store_frag(Bs[0], fb, b_kmaj, t);
-  __syncthreads();
+  // operand majorness per mode: A = H (K-major) or G (K-major for dH, MN-major for dW);
+  // B = W strip (K-major for the logits, MN-major for dH) or H (MN-major for dW)
+  Operand<MODE != MODE_DW> oa;
+  Operand<MODE == MODE_FWD_LSE || MODE == MODE_BWD_G> ob;
+  oa.init(p.A, p.a_sm, p.a_sk, m0, p.M, t);
+  ob.init(p.B, p.b_sn, p.b_sk, n0, p.Ncols, t);
+  float va[2][4], vb[2][4];
   const int nkb = (p.K + TK - 1) / TK;
+  oa.load(0, TK <= p.K, p.M, p.K, va);
+  ob.load(0, TK <= p.K, p.Ncols, p.K, vb);
+  oa.store(As[0], va, t);
+  ob.store(Bs[0], vb, t);
+  __syncthreads();
   for (int kb = 0; kb < nkb; ++kb) {
     const int cur = kb & 1;
     const bool more = kb + 1 < nkb;
     if (more) {  // next k-block into registers while this one is multiplied
-      load_frag(fa, p.A, p.a_sm, p.a_sk, a_kmaj, m0, (kb + 1) * TK, p.M, p.K, t);
-      load_frag(fb, p.B, p.b_sn, p.b_sk, b_kmaj, n0, (kb + 1) * TK, p.Ncols, p.K, t);
+      const bool kfull = (kb + 2) * TK <= p.K;
+      oa.base += oa.step;
+      ob.base += ob.step;
+      oa.load(kb + 1, kfull, p.M, p.K, va);
+      ob.load(kb + 1, kfull, p.Ncols, p.K, vb);
     }
 #pragma unroll
     for (int kk = 0; kk < TK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][kk][ty * 4]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][kk][64 + ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][kk][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][kk][64 + tx * 4]);
+      const int z = swz(kk);
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][kk][(ty * 4) ^ z]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][kk][(64 + ty * 4) ^ z]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][kk][(tx * 4) ^ z]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][kk][(64 + tx * 4) ^ z]);
       const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -151,8 +194,8 @@ __global__ void __launch_bounds__(THREADS, 2) simt_strip_kernel(const SParams p)
         for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
     if (more) {  // the other buffer was last read before the previous barrier
-      store_frag(As[cur ^ 1], fa, a_kmaj, t);
-      store_frag(Bs[cur ^ 1], fb, b_kmaj, t);
+      oa.store(As[cur ^ 1], va, t);
+      ob.store(Bs[cur ^ 1], vb, t);
     }
     __syncthreads();
   }
@@ -272,6 +315,16 @@ cudaError_t simt_strip_gemm(const StripArgs& s, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   if (p.M == 0 || p.Ncols == 0 || p.K == 0) return cudaSuccess;
+  // 32-bit index arithmetic in the kernel: fragment offsets of 64 rows (or 16 k-rows) of the
+  // largest stride, and tile-relative indices up to M + 255, N + 255, K + 31
+  const int64_t max_stride = std::max(std::max(p.a_sm, p.a_sk), std::max(p.b_sn, p.b_sk));
+  const int64_t kIntMax = 0x7fffffffLL;
+  if (64 * max_stride > kIntMax || p.M > kIntMax - 256 || p.Ncols > kIntMax - 256 ||
+      p.K > kIntMax - 64) {
+    set_error_detail("fp32 strip GEMM: shape beyond the engine's 32-bit indexing (M %d, N %d, K %d,"
+                     " stride %lld)", p.M, p.Ncols, p.K, static_cast<long long>(max_stride));
+    return cudaErrorInvalidValue;
+  }
   p.tiles_m = (p.M + TM - 1) / TM;
   p.tiles_n = (p.Ncols + TN - 1) / TN;
   if (static_cast<int64_t>(p.tiles_m) * p.tiles_n > 0x7fffffffLL) return cudaErrorInvalidValue;
