@@ -69,18 +69,20 @@ def tokens_per_second(world: int, tokens_per_rank: int, ms_per_step: float) -> f
 # SHA-256 is KERNEL_SOURCE_SHA256; once the source differs they no longer apply (traffic: null).
 KERNEL_SOURCES = ("memory_bounded_linear_gb300/csrc/lce_tc.cu",
                   "memory_bounded_linear_gb300/csrc/ptx.cuh",
-                  "memory_bounded_linear_gb300/csrc/lce_internal.h")
-KERNEL_SOURCE_SHA256 = "db13303ca53408257f62f7ca3cec55d05c602f417e9325dceafb056cd90d1b2e"
+                  "memory_bounded_linear_gb300/csrc/lce_internal.h",
+                  "memory_bounded_linear_gb300/csrc/lce_api.cu")  # launch structure
+KERNEL_SOURCE_SHA256 = "e57a8668a2aab9c5334dd7a09d5e76842c4fd60909dfd1172ca249edc07d362a"
 MEASURED_TRAFFIC = {
-    # N=32768 d=6144 V=151552, strip 16384: the timed step's 31 launches -- the forward over the
-    # whole vocabulary, then per strip the gradient, dH and dW launches (averaged over the 30)
-    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse", "bf16"): 30417206016,
-    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd", "bf16"): 7725515963,
+    # N=32768 d=6144 V=151552, strip 16384: the timed step's 21 launches -- the forward over the
+    # whole vocabulary, then per strip the gradient launch and the dW + dH launch (averaged
+    # over the 20)
+    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse", "bf16"): 30429322496,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd", "bf16"): 11722072192,
     # N=16384 d=7168 V=200000 fp32, three-product tf32, strip 16384: the timed step's 39
     # tensor-core launches -- 13 forward strips, then per strip the gradient launch and the
     # dH + dW launch (averaged over the 26)
-    ("n16384-d7168-v200000-fp32", 16384, "tc_fwd_lse", "tf32x3"): 14371110971,
-    ("n16384-d7168-v200000-fp32", 16384, "tc_bwd", "tf32x3"): 30438687379,
+    ("n16384-d7168-v200000-fp32", 16384, "tc_fwd_lse", "tf32x3"): 14170404627,
+    ("n16384-d7168-v200000-fp32", 16384, "tc_bwd", "tf32x3"): 26676866707,
 }
 
 

@@ -5,12 +5,12 @@
 //             (m, s) (+) (m', s') = (M, s e^(m - M) + s' e^(m' - M)),  M = max(m, m')
 //           ("Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training",
 //           section 3.2: each strip is folded into a running per-token state and released).
-//           Eight warps share the tiles of 32 tokens; coalesced over tokens.
+//           Eight warps share the tiles of 64 tokens; coalesced over tokens.
 // finalize: lse_i = m_i + log s_i for every row; per-token loss lse_i - t_i on valid rows; the
 //           sum over rows in a fixed order in fp64 (one block, fixed per-thread strides and a
 //           fixed tree), n_valid, and the label-range check.
 // split:    fp32 x -> tf32 parts hi = rna(x), lo = rna(x - hi) for the three-product tensor-core
-//           path (x = hi + lo + r with |r| about 2^-22 |x|); plain, or transposed through 32 x 32
+//           path (x = hi + lo + r with |r| about 2^-22 |x|); plain, or transposed through 64 x 64
 //           shared-memory tiles for the operands the tf32 MMAs need K-major.
 #include <cuda_runtime.h>
 #include <math.h>
@@ -30,28 +30,67 @@ __device__ __forceinline__ float2 fold(float2 a, float2 b) {
   return make_float2(M, a.y * expf(a.x - M) + b.y * expf(b.x - M));
 }
 
-// One block folds 32 consecutive tokens: warp w takes tiles w, w + 8, w + 16, ... of its lane's
-// token (coalesced over the 32 tokens), then lane j of warp 0 folds the eight warp states in warp
-// order and the result into the running state -- a fixed order, so the result is deterministic.
+// One block folds 64 consecutive tokens: lane j of every warp holds tokens 2j and 2j + 1 (one
+// 16-byte load per tile when N is even), warp w takes tiles w, w + 8, w + 16, ... and issues the
+// loads of four tiles before folding them (bytes in flight for HBM), folding in tile order.  Then
+// lane j of warp 0 folds the eight warp states in warp order and the result into the running
+// state -- a fixed order, so the result is deterministic.
 constexpr int COMBINE_WARPS = 8;
+constexpr int COMBINE_TOKENS = 64;
 
 __global__ void __launch_bounds__(COMBINE_WARPS * 32)
     combine_kernel(const float2* __restrict__ part, int tiles, int64_t N, float2* __restrict__ run,
                    int first) {
-  __shared__ float2 st_w[COMBINE_WARPS][32];
+  __shared__ float4 st_w[COMBINE_WARPS][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * 32 + lane;
-  float2 st = make_float2(-INFINITY, 0.f);
-  if (i < N)
-    for (int t = warp; t < tiles; t += COMBINE_WARPS)
-      st = fold(st, part[static_cast<size_t>(t) * N + i]);
-  st_w[warp][lane] = st;
-  __syncthreads();
-  if (warp == 0 && i < N) {
-    float2 acc = first ? make_float2(-INFINITY, 0.f) : run[i];
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * COMBINE_TOKENS + 2 * lane;
+  const bool has0 = i0 < N, has1 = i0 + 1 < N;
+  const bool vec = has1 && (N % 2 == 0);  // part + t * N + i0 is then 16-byte aligned
+  const float2 none = make_float2(-INFINITY, 0.f);
+  float2 a0 = none, a1 = none;
+  auto load2 = [&](int t, float2& x0, float2& x1) {
+    const float2* q = part + static_cast<size_t>(t) * N + i0;
+    if (vec) {
+      const float4 v = *reinterpret_cast<const float4*>(q);
+      x0 = make_float2(v.x, v.y);
+      x1 = make_float2(v.z, v.w);
+    } else {
+      x0 = q[0];
+      x1 = has1 ? q[1] : none;
+    }
+  };
+  if (has0) {
+    int t = warp;
+    for (; t + 3 * COMBINE_WARPS < tiles; t += 4 * COMBINE_WARPS) {
+      float2 x[4][2];
 #pragma unroll
-    for (int w = 0; w < COMBINE_WARPS; ++w) acc = fold(acc, st_w[w][lane]);
-    run[i] = acc;
+      for (int u = 0; u < 4; ++u) load2(t + u * COMBINE_WARPS, x[u][0], x[u][1]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a0 = fold(a0, x[u][0]);
+        a1 = fold(a1, x[u][1]);
+      }
+    }
+    for (; t < tiles; t += COMBINE_WARPS) {
+      float2 x0, x1;
+      load2(t, x0, x1);
+      a0 = fold(a0, x0);
+      a1 = fold(a1, x1);
+    }
+  }
+  st_w[warp][lane] = make_float4(a0.x, a0.y, a1.x, a1.y);
+  __syncthreads();
+  if (warp == 0 && has0) {
+    float2 r0 = first ? none : run[i0];
+    float2 r1 = (first || !has1) ? none : run[i0 + 1];
+#pragma unroll
+    for (int w = 0; w < COMBINE_WARPS; ++w) {
+      const float4 v = st_w[w][lane];
+      r0 = fold(r0, make_float2(v.x, v.y));
+      r1 = fold(r1, make_float2(v.z, v.w));
+    }
+    run[i0] = r0;
+    if (has1) run[i0 + 1] = r1;
   }
 }
 
@@ -121,33 +160,41 @@ __global__ void split_tf32_kernel(const float4* __restrict__ x, float4* __restri
   }
 }
 
-// Transposing split: x [rows x cols] -> hi / lo [cols x ld_out], one 32 x 32 tile at a time
-// (grid-stride over tiles); the tile row is padded by one word against bank conflicts, so both
-// the reads of x and the writes of hi / lo are coalesced.
-constexpr int TT = 32;
+// Transposing split: x [rows x cols] -> hi / lo [cols x ld_out], one 64 x 64 tile at a time
+// (grid-stride over tiles) through shared memory padded by one word against bank conflicts: each
+// thread issues its 16 loads of a tile before the barrier, and both the reads of x and the writes
+// of hi / lo are coalesced 128-byte rows.
+constexpr int TT = 64;
 
-__global__ void __launch_bounds__(TT * 8)
+__global__ void __launch_bounds__(32 * 8)
     split_tf32_t_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_out,
                         float* __restrict__ hi, float* __restrict__ lo) {
   __shared__ float t[TT][TT + 1];
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
   const int64_t tiles_c = (cols + TT - 1) / TT;
   const int64_t tiles = tiles_c * ((rows + TT - 1) / TT);
   for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int64_t r0 = (tile / tiles_c) * TT, c0 = (tile % tiles_c) * TT;
-    for (int i = threadIdx.y; i < TT; i += 8) {
-      const int64_t r = r0 + i, c = c0 + threadIdx.x;
-      t[i][threadIdx.x] = (r < rows && c < cols) ? x[r * cols + c] : 0.f;
-    }
-    __syncthreads();
-    for (int i = threadIdx.y; i < TT; i += 8) {
-      const int64_t c = c0 + i, r = r0 + threadIdx.x;
-      if (c < cols && r < rows) {
-        const float v = t[threadIdx.x][i];
-        const float h = round_tf32(v);
-        hi[c * ld_out + r] = h;
-        lo[c * ld_out + r] = round_tf32(v - h);
+#pragma unroll
+    for (int i = 0; i < TT / 8; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t r = r0 + ty + 8 * i, c = c0 + tx + 32 * h;
+        t[ty + 8 * i][tx + 32 * h] = (r < rows && c < cols) ? x[r * cols + c] : 0.f;
       }
-    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < TT / 8; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t c = c0 + ty + 8 * i, r = r0 + tx + 32 * h;
+        if (c < cols && r < rows) {
+          const float v = t[tx + 32 * h][ty + 8 * i];
+          const float hv = round_tf32(v);
+          hi[c * ld_out + r] = hv;
+          lo[c * ld_out + r] = round_tf32(v - hv);
+        }
+      }
     __syncthreads();
   }
 }
@@ -176,7 +223,7 @@ cudaError_t launch_split_tf32_t(const float* x, int64_t rows, int64_t cols, int6
   if (ld_out < rows) return cudaErrorInvalidValue;
   const int64_t tiles = ((rows + TT - 1) / TT) * ((cols + TT - 1) / TT);
   const int64_t blocks = tiles < kSplitMaxBlocks ? tiles : kSplitMaxBlocks;
-  split_tf32_t_kernel<<<static_cast<unsigned>(blocks), dim3(TT, 8), 0, stream>>>(x, rows, cols,
+  split_tf32_t_kernel<<<static_cast<unsigned>(blocks), dim3(32, 8), 0, stream>>>(x, rows, cols,
                                                                                 ld_out, hi, lo);
   return cudaGetLastError();
 }
@@ -184,7 +231,7 @@ cudaError_t launch_split_tf32_t(const float* x, int64_t rows, int64_t cols, int6
 cudaError_t launch_combine(const float2* part, int tiles, int64_t N, float2* run, int first,
                            cudaStream_t stream) {
   if (N == 0) return cudaSuccess;
-  const int64_t blocks = (N + 31) / 32;
+  const int64_t blocks = (N + COMBINE_TOKENS - 1) / COMBINE_TOKENS;
   combine_kernel<<<static_cast<unsigned>(blocks), COMBINE_WARPS * 32, 0, stream>>>(part, tiles, N,
                                                                                  run, first);
   return cudaGetLastError();
