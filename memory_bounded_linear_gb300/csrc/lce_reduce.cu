@@ -32,11 +32,13 @@ __device__ __forceinline__ float2 fold(float2 a, float2 b) {
 
 // One block folds 64 consecutive tokens: lane j of every warp holds tokens 2j and 2j + 1 (one
 // 16-byte load per tile when N is even), warp w takes tiles w, w + 8, w + 16, ... and issues the
-// loads of four tiles before folding them (bytes in flight for HBM), folding in tile order.  Then
+// loads of COMBINE_BATCH tiles before folding them (bytes in flight for HBM), folding in tile
+// order.  Then
 // lane j of warp 0 folds the eight warp states in warp order and the result into the running
 // state -- a fixed order, so the result is deterministic.
 constexpr int COMBINE_WARPS = 8;
 constexpr int COMBINE_TOKENS = 64;
+constexpr int COMBINE_BATCH = 8;
 
 __global__ void __launch_bounds__(COMBINE_WARPS * 32)
     combine_kernel(const float2* __restrict__ part, int tiles, int64_t N, float2* __restrict__ run,
@@ -61,12 +63,12 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32)
   };
   if (has0) {
     int t = warp;
-    for (; t + 3 * COMBINE_WARPS < tiles; t += 4 * COMBINE_WARPS) {
-      float2 x[4][2];
+    for (; t + (COMBINE_BATCH - 1) * COMBINE_WARPS < tiles; t += COMBINE_BATCH * COMBINE_WARPS) {
+      float2 x[COMBINE_BATCH][2];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) load2(t + u * COMBINE_WARPS, x[u][0], x[u][1]);
+      for (int u = 0; u < COMBINE_BATCH; ++u) load2(t + u * COMBINE_WARPS, x[u][0], x[u][1]);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < COMBINE_BATCH; ++u) {
         a0 = fold(a0, x[u][0]);
         a1 = fold(a1, x[u][1]);
       }
