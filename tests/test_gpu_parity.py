@@ -175,35 +175,50 @@ def test_all_rows_ignored(cuda_lib):
     assert np.max(np.abs(g["lse"] - r["lse"]) / np.abs(r["lse"])) < 1e-3
 
 
-def test_custom_ignore_index(cuda_lib):
-    w = W3.with_sizes(N=300, d=96, V=900, strip_V=256)
+# (input format, f32_mode): bf16 on the tensor cores, fp32 exact on the CUDA cores, fp32 as three
+# tf32 products on the tensor cores
+FORMATS = [("bf16", "exact"), ("f32", "exact"), ("f32", "tf32x3")]
+FORMAT_IDS = ["bf16", "f32", "tf32x3"]
+
+
+def _as_format(w, fmt):
+    """The same workload distributions with H and W in the given input format."""
+    return w if fmt == w.dtype else w.with_sizes(dtype=fmt)
+
+
+@pytest.mark.parametrize("fmt,mode", FORMATS, ids=FORMAT_IDS)
+def test_custom_ignore_index(cuda_lib, fmt, mode):
+    w = _as_format(W3.with_sizes(N=300, d=96, V=900, strip_V=256), fmt)
     H, W, y = make_inputs(w, "cpu")
     y[y == -100] = 7  # the ignored rows now carry label 7, which is the ignore_index below
-    g = run_gpu(H, W, y, 256, "mean", ignore_index=7)
+    g = run_gpu(H, W, y, 256, "mean", ignore_index=7, f32_mode=mode)
     r = run_oracle(H, W, y, "mean", ignore_index=7)
-    assert_parity(g, r, "bf16")
+    assert_parity(g, r, "tf32x3" if mode == "tf32x3" else fmt)
 
 
-def test_bad_label_is_reported_and_row_excluded(cuda_lib):
-    w = W2.with_sizes(N=300, d=64, V=600, strip_V=256)
+@pytest.mark.parametrize("fmt,mode", FORMATS, ids=FORMAT_IDS)
+def test_bad_label_is_reported_and_row_excluded(cuda_lib, fmt, mode):
+    w = _as_format(W2.with_sizes(N=300, d=64, V=600, strip_V=256), fmt)
     H, W, y = make_inputs(w, "cpu")
     y[5] = 600      # == V
     y[17] = -3      # negative, not ignore_index
+    y[290] = 10**9  # far out of range, in the last row tile
     with pytest.raises(LceError) as e:
-        run_gpu(H, W, y, 256, "mean")
+        run_gpu(H, W, y, 256, "mean", f32_mode=mode)
     assert e.value.name == "LCE_ERR_LABEL_OUT_OF_RANGE"
-    g = run_gpu(H, W, y, 256, "mean", check=False)
+    g = run_gpu(H, W, y, 256, "mean", check=False, f32_mode=mode)
     r = run_oracle(H, W, y, "mean")
-    assert r["n_valid"] == 298
-    assert_parity(g, r, "bf16")
-    assert np.all(g["dH"][[5, 17]] == 0)
+    assert r["n_valid"] == 297
+    assert_parity(g, r, "tf32x3" if mode == "tf32x3" else fmt)
+    assert np.all(g["dH"][[5, 17, 290]] == 0)
 
 
-def test_bitwise_deterministic(cuda_lib):
-    w = W5.with_sizes(N=700, d=192, V=3000, strip_V=1024)
+@pytest.mark.parametrize("fmt,mode", FORMATS, ids=FORMAT_IDS)
+def test_bitwise_deterministic(cuda_lib, fmt, mode):
+    w = _as_format(W5.with_sizes(N=700, d=192, V=3000, strip_V=1024), fmt)
     H, W, y = make_inputs(w, "cpu")
-    a = run_gpu(H, W, y, 1024, "sum")
-    b = run_gpu(H, W, y, 1024, "sum")
+    a = run_gpu(H, W, y, 1024, "sum", f32_mode=mode)
+    b = run_gpu(H, W, y, 1024, "sum", f32_mode=mode)
     assert a["loss"] == b["loss"]
     for k in ("lse", "dH", "dW"):
         assert np.array_equal(a[k], b[k]), k
@@ -235,6 +250,22 @@ def test_autograd_function_matches(cuda_lib):
     assert Hd.grad.dtype == torch.bfloat16 and Wd.grad.dtype == torch.bfloat16
     assert rel_fro(Hd.grad.double().cpu().numpy(), r["dH"]) <= 1.5e-2
     assert rel_fro(Wd.grad.double().cpu().numpy(), r["dW"]) <= 1.5e-2
+
+
+def test_autograd_function_tf32x3(cuda_lib):
+    """fp32 tensors through the autograd function on the tensor-core fp32 path: fp32 gradients at
+    the fp32 tolerances."""
+    w = WT.with_sizes(N=333, d=128, V=1500, strip_V=512)
+    H, W, y = make_inputs(w, "cpu")
+    Hd = H.cuda().requires_grad_(True)
+    Wd = W.cuda().requires_grad_(True)
+    loss = api.linear_cross_entropy(Hd, Wd, y.cuda(), strip_V=512, f32_mode="tf32x3")
+    loss.backward()
+    r = run_oracle(H, W, y, "mean")
+    assert abs(loss.item() - r["loss"]) <= 1e-5 * abs(r["loss"])
+    assert Hd.grad.dtype == torch.float32 and Wd.grad.dtype == torch.float32
+    assert rel_fro(Hd.grad.double().cpu().numpy(), r["dH"]) <= 1e-4
+    assert rel_fro(Wd.grad.double().cpu().numpy(), r["dW"]) <= 1e-4
 
 
 def test_workspace_bound_and_peak_memory(cuda_lib):
