@@ -71,7 +71,7 @@ KERNEL_SOURCES = ("memory_bounded_linear_gb300/csrc/lce_tc.cu",
                   "memory_bounded_linear_gb300/csrc/ptx.cuh",
                   "memory_bounded_linear_gb300/csrc/lce_internal.h",
                   "memory_bounded_linear_gb300/csrc/lce_api.cu")  # launch structure
-KERNEL_SOURCE_SHA256 = "e57a8668a2aab9c5334dd7a09d5e76842c4fd60909dfd1172ca249edc07d362a"
+KERNEL_SOURCE_SHA256 = "0aeb093c9d5fa2ad3010232484b5323835e32d3cb317202af2b5d32d25f96799"
 MEASURED_TRAFFIC = {
     # N=32768 d=6144 V=151552, strip 16384: the timed step's 21 launches -- the forward over the
     # whole vocabulary, then per strip the gradient launch and the dW + dH launch (averaged

@@ -417,19 +417,11 @@ lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* lab
       for (int64_t s = 0; s < S; ++s) {
         StripArgs grad = strip_job(s, MODE_BWD_G, G);
         if (run(&grad, 1) != cudaSuccess) return LCE_ERR_CUDA;
-#ifdef LCE_BWD_SEPARATE_DH_DW
-        for (int mode : {MODE_DH, MODE_DW}) {
-          if ((mode == MODE_DH && !want_dh) || (mode == MODE_DW && !want_dw)) continue;
-          StripArgs job = strip_job(s, mode, G);
-          if (run(&job, 1) != cudaSuccess) return LCE_ERR_CUDA;
-        }
-#else
         StripArgs jobs[2];
         int nj = 0;
         if (want_dw) jobs[nj++] = strip_job(s, MODE_DW, G);
         if (want_dh) jobs[nj++] = strip_job(s, MODE_DH, G);
         if (run(jobs, nj) != cudaSuccess) return LCE_ERR_CUDA;
-#endif
       }
     }
     return LCE_OK;
