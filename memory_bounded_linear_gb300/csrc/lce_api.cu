@@ -162,9 +162,11 @@ cudaError_t traced(int kid, cudaStream_t stream, F&& launch) {
   // check after the launch reports only this launch (sticky errors are reported again anyway).
   (void)cudaGetLastError();
   g_detail_set = false;
+  g_extra_kernels = 0;
   cudaError_t e = note(launch());
   if (e != cudaSuccess) return e;
-  g_launches.fetch_add(1, std::memory_order_relaxed);
+  g_launches.fetch_add(1 + g_extra_kernels, std::memory_order_relaxed);
+  g_extra_kernels = 0;
   if (rec) {
     e = cudaEventRecord(static_cast<cudaEvent_t>(g_trace.stop[g_trace.n]), stream);
     if (e != cudaSuccess) return e;
@@ -228,6 +230,8 @@ void set_x3_operands(StripArgs& a, char* ws, const Layout& L) {
 }
 
 }  // namespace
+
+thread_local int g_extra_kernels = 0;
 
 void set_error_detail(const char* fmt, ...) {
   va_list ap;

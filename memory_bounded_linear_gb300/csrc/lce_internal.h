@@ -74,6 +74,9 @@ struct StripArgs {
   int64_t ldt;  // row stride (elements) of HT and GT: N rounded up to a multiple of 32
 };
 
+// Kernels a launcher started beyond its first one (the launch counter adds them), per thread.
+extern thread_local int g_extra_kernels;
+
 // Records a human-readable description of the last failure on the calling thread (reported by
 // lce_last_cuda_error).  printf-style.
 void set_error_detail(const char* fmt, ...);
@@ -100,7 +103,9 @@ cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, size_t n, cu
 // The same split of x [rows x cols] (row-major), written transposed: hi / lo [cols x ld_out].
 cudaError_t launch_split_tf32_t(const float* x, int64_t rows, int64_t cols, int64_t ld_out,
                                 float* hi, float* lo, cudaStream_t stream);
-cudaError_t launch_combine(const float2* part, int tiles, int64_t N, float2* run, int first,
+// Folds the per-(tile, row) partials of one strip into the running state; may overwrite
+// partials (they are consumed).
+cudaError_t launch_combine(float2* part, int tiles, int64_t N, float2* run, int first,
                            cudaStream_t stream);
 cudaError_t launch_finalize(const float2* run, const float* tgt, const int64_t* labels,
                             int64_t N, int64_t V, int64_t ignore_index, int reduction,

@@ -16,6 +16,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "lce_internal.h"
 #include "ptx.cuh"
 
@@ -30,22 +32,26 @@ __device__ __forceinline__ float2 fold(float2 a, float2 b) {
   return make_float2(M, a.y * expf(a.x - M) + b.y * expf(b.x - M));
 }
 
-// One block folds 64 consecutive tokens: lane j of every warp holds tokens 2j and 2j + 1 (one
-// 16-byte load per tile when N is even), warp w takes tiles w, w + 8, w + 16, ... and issues the
-// loads of COMBINE_BATCH tiles before folding them (bytes in flight for HBM), folding in tile
-// order.  Then
-// lane j of warp 0 folds the eight warp states in warp order and the result into the running
-// state -- a fixed order, so the result is deterministic.
+// One block folds 64 consecutive tokens over one chunk of the tiles: lane j of every warp holds
+// tokens 2j and 2j + 1 (one 16-byte load per tile when N is even), warp w takes the chunk's tiles
+// w, w + 8, w + 16, ... and issues the loads of COMBINE_BATCH tiles before folding them (bytes in
+// flight for HBM), folding in tile order.  Then lane j of warp 0 folds the eight warp states in
+// warp order.  With one chunk the result goes into the running state; with several (few tokens,
+// so few blocks), each block writes its chunk's state over the chunk's first partial slot and
+// combine_chunks_kernel folds the chunks in order.  Every order is fixed by N and the tile count,
+// so the result is deterministic.
 constexpr int COMBINE_WARPS = 8;
 constexpr int COMBINE_TOKENS = 64;
 constexpr int COMBINE_BATCH = 8;
 
 __global__ void __launch_bounds__(COMBINE_WARPS * 32)
-    combine_kernel(const float2* __restrict__ part, int tiles, int64_t N, float2* __restrict__ run,
-                   int first) {
+    combine_kernel(float2* __restrict__ part, int tiles, int chunk_tiles, int chunks, int64_t N,
+                   float2* __restrict__ run, int first) {
   __shared__ float4 st_w[COMBINE_WARPS][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * COMBINE_TOKENS + 2 * lane;
+  const int t_begin = static_cast<int>(blockIdx.y) * chunk_tiles;
+  const int t_end = min(tiles, t_begin + chunk_tiles);
   const bool has0 = i0 < N, has1 = i0 + 1 < N;
   const bool vec = has1 && (N % 2 == 0);  // part + t * N + i0 is then 16-byte aligned
   const float2 none = make_float2(-INFINITY, 0.f);
@@ -62,8 +68,8 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32)
     }
   };
   if (has0) {
-    int t = warp;
-    for (; t + (COMBINE_BATCH - 1) * COMBINE_WARPS < tiles; t += COMBINE_BATCH * COMBINE_WARPS) {
+    int t = t_begin + warp;
+    for (; t + (COMBINE_BATCH - 1) * COMBINE_WARPS < t_end; t += COMBINE_BATCH * COMBINE_WARPS) {
       float2 x[COMBINE_BATCH][2];
 #pragma unroll
       for (int u = 0; u < COMBINE_BATCH; ++u) load2(t + u * COMBINE_WARPS, x[u][0], x[u][1]);
@@ -73,7 +79,7 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32)
         a1 = fold(a1, x[u][1]);
       }
     }
-    for (; t < tiles; t += COMBINE_WARPS) {
+    for (; t < t_end; t += COMBINE_WARPS) {
       float2 x0, x1;
       load2(t, x0, x1);
       a0 = fold(a0, x0);
@@ -81,19 +87,32 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32)
     }
   }
   st_w[warp][lane] = make_float4(a0.x, a0.y, a1.x, a1.y);
-  __syncthreads();
+  __syncthreads();  // every read of this block's partials is done before slot t_begin is reused
   if (warp == 0 && has0) {
-    float2 r0 = first ? none : run[i0];
-    float2 r1 = (first || !has1) ? none : run[i0 + 1];
+    const bool direct = (chunks == 1);
+    float2 r0 = (first || !direct) ? none : run[i0];
+    float2 r1 = (first || !direct || !has1) ? none : run[i0 + 1];
 #pragma unroll
     for (int w = 0; w < COMBINE_WARPS; ++w) {
       const float4 v = st_w[w][lane];
       r0 = fold(r0, make_float2(v.x, v.y));
       r1 = fold(r1, make_float2(v.z, v.w));
     }
-    run[i0] = r0;
-    if (has1) run[i0 + 1] = r1;
+    float2* out = direct ? run + i0 : part + static_cast<size_t>(t_begin) * N + i0;
+    out[0] = r0;
+    if (has1) out[1] = r1;
   }
+}
+
+// Second pass of a chunked combine: token i folds its chunk states in chunk order.
+__global__ void combine_chunks_kernel(const float2* __restrict__ part, int chunk_tiles, int chunks,
+                                      int64_t N, float2* __restrict__ run, int first) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  float2 acc = first ? make_float2(-INFINITY, 0.f) : run[i];
+  for (int c = 0; c < chunks; ++c)
+    acc = fold(acc, part[static_cast<size_t>(c) * chunk_tiles * N + i]);
+  run[i] = acc;
 }
 
 constexpr int FIN_THREADS = 1024;
@@ -230,12 +249,25 @@ cudaError_t launch_split_tf32_t(const float* x, int64_t rows, int64_t cols, int6
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const float2* part, int tiles, int64_t N, float2* run, int first,
+cudaError_t launch_combine(float2* part, int tiles, int64_t N, float2* run, int first,
                            cudaStream_t stream) {
-  if (N == 0) return cudaSuccess;
-  const int64_t blocks = (N + COMBINE_TOKENS - 1) / COMBINE_TOKENS;
-  combine_kernel<<<static_cast<unsigned>(blocks), COMBINE_WARPS * 32, 0, stream>>>(part, tiles, N,
-                                                                                 run, first);
+  if (N == 0 || tiles < 1) return cudaSuccess;
+  // Fewer token blocks than the 152 SMs of a GB300: the tiles are split into chunks (at least 8
+  // tiles each, so every warp has one) until there are about two blocks per SM.  The chunking
+  // depends on N and the tile count only.
+  const int64_t token_blocks = (N + COMBINE_TOKENS - 1) / COMBINE_TOKENS;
+  int64_t want = (token_blocks < 152) ? (2 * 152 + token_blocks - 1) / token_blocks : 1;
+  want = std::min<int64_t>(want, std::max(1, tiles / 8));
+  const int chunk_tiles = static_cast<int>((tiles + want - 1) / want);
+  const int chunks = (tiles + chunk_tiles - 1) / chunk_tiles;
+  combine_kernel<<<dim3(static_cast<unsigned>(token_blocks), static_cast<unsigned>(chunks)),
+                   COMBINE_WARPS * 32, 0, stream>>>(part, tiles, chunk_tiles, chunks, N, run, first);
+  if (chunks > 1) {
+    ++g_extra_kernels;
+    const int threads = 256;
+    combine_chunks_kernel<<<static_cast<unsigned>((N + threads - 1) / threads), threads, 0,
+                            stream>>>(part, chunk_tiles, chunks, N, run, first);
+  }
   return cudaGetLastError();
 }
 
