@@ -77,8 +77,9 @@ typedef enum { LCE_BF16 = 0, LCE_F32 = 1, LCE_F32_TF32X3 = 2 } lce_dtype_t;
 
 /*
  * Bytes of device workspace that lce_forward and lce_backward need for these sizes; 0 when the
- * arguments break a shape rule.  It grows as O(N * min(strip_V, V)) and never with V beyond the
- * strip: this is the closed-form per-call budget that can be checked before launch
+ * arguments break a shape rule.  It grows as O(N * min(strip_V, V)) (LCE_F32_TF32X3 adds
+ * O((N + min(strip_V, V)) * d) for its operand copies) and never with V beyond the strip: this
+ * is the closed-form per-call budget that can be checked before launch
  * ("Flattening Every Memory Peak in Long-Context Mixture-of-Experts Training", sections 3.5
  * and 6: the per-rank budget is fixed by the launch configuration).  Layout: a 256-byte header
  * (error flags) followed by the larger of the forward region (running state, target logits,
@@ -95,7 +96,7 @@ size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_
 
 /*
  * Forward.  Visits the vocabulary in strips of strip_V columns; for each strip it forms the
- * logit tiles on the tensor cores, folds them into the running per-token state in the GEMM
+ * logit tiles (tensor cores; CUDA cores for LCE_F32), folds them into the running per-token state in the GEMM
  * epilogue and drops them.  Writes
  *   loss    : device fp32 scalar (MEAN over valid rows; NaN when n_valid == 0.  SUM: the sum)
  *   lse     : device fp32 [N], log-sum-exp of every row (ignored rows included)
@@ -113,7 +114,8 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels,
  * labels) and the incoming gradient dloss (device fp32 scalar).  For each strip it recomputes
  * the logits, forms G = scale * (softmax - onehot) in the epilogue (scale = dloss / n_valid for
  * MEAN, dloss for SUM) into one strip of workspace, then accumulates dH += G_s W_s and writes
- * dW_s = G_s^T H on the tensor cores.  Writes dH (device fp32 [N x d], overwritten) and dW
+ * dW_s = G_s^T H (tensor cores; CUDA cores for LCE_F32).  Writes dH (device fp32 [N x d],
+ * overwritten) and dW
  * (device fp32 [V x d], overwritten).  dW rows are each written exactly once (deterministic).
  * The workspace need not come from lce_forward; its header (error flags) is cleared first, so
  * lce_check_error afterwards reports the problems this call found.
