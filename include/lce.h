@@ -96,8 +96,8 @@ size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_
 
 /*
  * Forward.  Visits the vocabulary in strips of strip_V columns; for each strip it forms the
- * logit tiles (tensor cores; CUDA cores for LCE_F32), folds them into the running per-token state in the GEMM
- * epilogue and drops them.  Writes
+ * logit tiles (tensor cores; CUDA cores for LCE_F32), folds them into the running per-token
+ * state in the GEMM epilogue and drops them.  Writes
  *   loss    : device fp32 scalar (MEAN over valid rows; NaN when n_valid == 0.  SUM: the sum)
  *   lse     : device fp32 [N], log-sum-exp of every row (ignored rows included)
  *   n_valid : device int64 scalar, number of rows whose label is in [0, V)
@@ -115,8 +115,8 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels,
  * the logits, forms G = scale * (softmax - onehot) in the epilogue (scale = dloss / n_valid for
  * MEAN, dloss for SUM) into one strip of workspace, then accumulates dH += G_s W_s and writes
  * dW_s = G_s^T H (tensor cores; CUDA cores for LCE_F32).  Writes dH (device fp32 [N x d],
- * overwritten) and dW
- * (device fp32 [V x d], overwritten).  dW rows are each written exactly once (deterministic).
+ * overwritten) and dW (device fp32 [V x d], overwritten).  dW rows are each written exactly once
+ * (deterministic).
  * The workspace need not come from lce_forward; its header (error flags) is cleared first, so
  * lce_check_error afterwards reports the problems this call found.
  */
