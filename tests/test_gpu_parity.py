@@ -315,3 +315,19 @@ def test_backward_parts_match_fused_bitwise(cuda_lib, w, mode):
     tol = 1e-2 if w.dtype == "bf16" else 1e-4
     assert rel_fro(dH1.cpu().double().numpy(), r["dH"]) <= tol
     assert rel_fro(dW2.cpu().double().numpy(), r["dW"]) <= tol
+
+
+@pytest.mark.parametrize("mode", ["exact", "tf32x3"])
+def test_backward_parts_empty_batch(cuda_lib, mode):
+    """No token: the dW-only call writes dW = 0, the dH-only call has nothing to write."""
+    w = (W2 if mode == "exact" else WT).with_sizes(N=0, d=64, V=300, strip_V=128)
+    H, W, y = make_inputs(w, "cuda")
+    kw = dict(strip_V=128, f32_mode=mode)
+    loss, lse, nv, ws = api.lce_forward(H, W, y, **kw)
+    one = torch.ones((), device="cuda")
+    dW = torch.full((300, 64), 7.0, device="cuda")
+    _, dW2, _ = api.lce_backward(H, W, y, lse, nv, one, workspace=ws, dW=dW, parts="dw", **kw)
+    dH1, _, _ = api.lce_backward(H, W, y, lse, nv, one, workspace=ws, parts="dh", **kw)
+    api.lce_check_error(ws)
+    assert torch.count_nonzero(dW2).item() == 0
+    assert dH1.shape == (0, 64)
