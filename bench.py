@@ -490,6 +490,32 @@ def main():
                      "wgrad_only_ms": bwd_ms["dw"], "iterations": n_bwd,
                      "critical_path_fraction": bwd_ms["dh"] / bwd_ms["both"]}
 
+    # The same step captured once into a CUDA graph and replayed K times (no host work per step):
+    # the launch overhead the direct calls above pay shows as the difference.
+    def step_current_stream():
+        api.lce_forward(H, W, y, strip_V=S, reduction=w.reduction, workspace=ws,
+                        out=(loss, lse, nv), f32_mode=fm)
+        api.lce_backward(H, W, y, lse, nv, one, strip_V=S, reduction=w.reduction, workspace=ws,
+                         dH=dH, dW=dW, f32_mode=fm)
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step_current_stream()
+    graph.replay()
+    barrier()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record(stream)
+    barrier()
+    api.lce_check_error(ws)
+    graph_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, world, dev)
+    cuda_graph = {"ms_per_step": graph_ms, "value": tokens_per_second(world, N, graph_ms),
+                  "unit": "tokens/s"}
+    del graph
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, H, W, y)
@@ -516,6 +542,7 @@ def main():
             "clocks": clk,
             "e2e": e2e,
             "delayed_wgrad": delayed_wgrad,
+            "cuda_graph": cuda_graph,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
