@@ -491,30 +491,44 @@ def main():
                      "critical_path_fraction": bwd_ms["dh"] / bwd_ms["both"]}
 
     # The same step captured once into a CUDA graph and replayed K times (no host work per step):
-    # the launch overhead the direct calls above pay shows as the difference.
+    # any launch overhead the direct calls above pay would show as the difference.
     def step_current_stream():
         api.lce_forward(H, W, y, strip_V=S, reduction=w.reduction, workspace=ws,
                         out=(loss, lse, nv), f32_mode=fm)
         api.lce_backward(H, W, y, lse, nv, one, strip_V=S, reduction=w.reduction, workspace=ws,
                          dH=dH, dW=dW, f32_mode=fm)
 
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step_current_stream()
-    graph.replay()
-    barrier()
-    g0 = torch.cuda.Event(enable_timing=True)
-    g1 = torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    for _ in range(args.steps):
+    # (thread-local capture: other threads of the process -- e.g. a process group's watchdog --
+    # may keep using CUDA meanwhile)
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            step_current_stream()
         graph.replay()
-    g1.record(stream)
+        graph_err = None
+    except RuntimeError as ex:
+        graph, graph_err = None, str(ex).splitlines()[0][:200]
+    # every rank times the replays, or none does (the barriers below must match across ranks)
+    if max_over_ranks(0.0 if graph_err is None else 1.0, world, dev) > 0.0:
+        graph_err = graph_err or "capture failed on another rank"
+        graph = None
     barrier()
-    api.lce_check_error(ws)
-    graph_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, world, dev)
-    cuda_graph = {"ms_per_step": graph_ms, "value": tokens_per_second(world, N, graph_ms),
-                  "unit": "tokens/s"}
-    del graph
+    if graph is not None:
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(stream)
+        barrier()
+        api.lce_check_error(ws)
+        t_graph = g0.elapsed_time(g1) / args.steps
+        del graph
+    else:
+        t_graph = float("nan")
+    graph_ms = max_over_ranks(t_graph, world, dev)
+    cuda_graph = ({"ms_per_step": graph_ms, "value": tokens_per_second(world, N, graph_ms),
+                   "unit": "tokens/s"} if graph_err is None else {"unavailable": graph_err})
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
