@@ -331,3 +331,28 @@ def test_backward_parts_empty_batch(cuda_lib, mode):
     api.lce_check_error(ws)
     assert torch.count_nonzero(dW2).item() == 0
     assert dH1.shape == (0, 64)
+
+
+def _random_shapes(seed, count):
+    """Seeded random small shapes: odd token counts, hidden sizes of any multiple of 8, vocabulary
+    sizes with ragged tails, strip widths of 128..1024, both reductions."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        N = int(rng.integers(1, 900))
+        d = 8 * int(rng.integers(1, 48))
+        V = int(rng.integers(2, 4000))
+        strip = 128 * int(rng.integers(1, 9))
+        red = "sum" if rng.random() < 0.5 else "mean"
+        out.append((N, d, V, strip, red))
+    return out
+
+
+@pytest.mark.parametrize("fmt,mode", FORMATS, ids=FORMAT_IDS)
+def test_random_shapes(cuda_lib, fmt, mode):
+    """Eight seeded random shapes per input format, each against the oracle at its tolerances."""
+    base = W2 if fmt == "bf16" else WT
+    seed = 20261202 + {"bf16": 1, "f32": 2}[fmt] + (10 if mode == "tf32x3" else 0)
+    for N, d, V, strip, red in _random_shapes(seed, 8):
+        w = base.with_sizes(N=N, d=d, V=V, strip_V=strip, reduction=red)
+        parity_case(w, f32_mode=mode)
