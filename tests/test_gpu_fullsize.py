@@ -123,3 +123,20 @@ def test_n16384_d7168_v200000_fp32_tf32x3_strip16384(cuda_lib):
     tolerances."""
     _check(WORKLOADS["n16384-d7168-v200000-fp32"], 16384, full_lse=False, n_rows=24, n_vocab=0,
            f32_mode="tf32x3")
+
+
+def test_n4096_d2048_v151936_single_cta_tiles(cuda_lib):
+    """The single-CTA 128x256 tile variant at a full benchmark shape (the default picks CTA
+    pairs here): the same sampled checks."""
+    assert cuda_lib.lce_set_tile_config(1) == 0
+    try:
+        _check(WORKLOADS["n4096-d2048-v151936"], 8192, full_lse=True)
+    finally:
+        cuda_lib.lce_set_tile_config(0)
+
+
+def test_n4096_d2048_v151936_fp32_tf32x3_strip8192(cuda_lib):
+    """fp32 inputs at the N=4096 shape on the tensor cores: 19 strips of the split-and-launch
+    loop, exact loss and sampled dW rows against the oracle's full lse, fp32 tolerances."""
+    w = WORKLOADS["n4096-d2048-v151936"].with_sizes(dtype="f32")
+    _check(w, 8192, full_lse=True, f32_mode="tf32x3")
