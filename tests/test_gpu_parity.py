@@ -356,3 +356,27 @@ def test_random_shapes(cuda_lib, fmt, mode):
     for N, d, V, strip, red in _random_shapes(seed, 8):
         w = base.with_sizes(N=N, d=d, V=V, strip_V=strip, reduction=red)
         parity_case(w, f32_mode=mode)
+
+
+@pytest.mark.parametrize("mode", ["exact", "tf32x3"])
+def test_dgrad_and_wgrad_on_two_streams(cuda_lib, mode):
+    """The delayed weight gradient in use: dH on one stream and dW on another, in flight together
+    (each call with its own workspace), give bitwise the fused backward's dH and dW."""
+    w = (W2 if mode == "exact" else WT).with_sizes(N=2048, d=256, V=5000, strip_V=1024)
+    H, W, y = make_inputs(w, "cuda")
+    kw = dict(strip_V=w.strip_V, reduction=w.reduction, f32_mode=mode)
+    loss, lse, nv, ws = api.lce_forward(H, W, y, **kw)
+    one = torch.ones((), device="cuda")
+    dH_ref, dW_ref, _ = api.lce_backward(H, W, y, lse, nv, one, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    ws2 = torch.empty_like(ws)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for s in (s1, s2):
+        s.wait_stream(torch.cuda.current_stream())
+    dH, _, _ = api.lce_backward(H, W, y, lse, nv, one, workspace=ws, parts="dh", stream=s1, **kw)
+    _, dW, _ = api.lce_backward(H, W, y, lse, nv, one, workspace=ws2, parts="dw", stream=s2, **kw)
+    torch.cuda.synchronize()
+    api.lce_check_error(ws)
+    api.lce_check_error(ws2)
+    assert torch.equal(dH, dH_ref)
+    assert torch.equal(dW, dW_ref)
