@@ -988,6 +988,12 @@ bool make_job(const StripArgs& s, TcMaps& maps, Job& jb, int j) {
   jb.tiles_m = (M + Cf::TILE_M - 1) / Cf::TILE_M;
   jb.tiles_n = (Ncols + BN - 1) / BN;
   jb.nkb = (K + BK - 1) / BK;
+  // tiles are numbered with 32-bit tickets
+  if (static_cast<int64_t>(jb.tiles_m) * jb.tiles_n > (int64_t(1) << 30)) {
+    set_error_detail("strip GEMM of %d x %d tiles: beyond the tile scheduler's range", jb.tiles_m,
+                     jb.tiles_n);
+    return false;
+  }
   jb.num_tiles = (jb.nkb > 0) ? jb.tiles_m * jb.tiles_n : 0;
   jb.strip_cols = s.strip_cols;
   jb.col0 = s.col0;
@@ -1007,6 +1013,7 @@ cudaError_t run(const StripArgs* jobs, int njobs, cudaStream_t stream, int num_s
     if (!make_job<PAIR, OP>(jobs[i], maps, jb, p.njobs)) return cudaErrorInvalidResourceHandle;
     if (jb.num_tiles == 0) continue;  // nothing to compute (e.g. an empty dimension)
     p.job[p.njobs++] = jb;
+    if (p.total_tiles > (1 << 30) - jb.num_tiles) return cudaErrorInvalidValue;  // 32-bit tickets
     p.total_tiles += jb.num_tiles;
   }
   if (p.njobs == 0) return cudaSuccess;
