@@ -372,12 +372,16 @@ def main():
     # kernel's tensor work is 3x its fp32 GEMM FLOPs, set against the tf32 peak (the measured bf16
     # peak x the nominal dense tf32 / bf16 ratio, 18 / 36 PFLOP/s per 8 GPUs)
     x3_factor = 3 if dt == "tf32x3" else 1
+    # The sustained peak (back-to-back GEMMs held at the power cap) when the power cap was active
+    # during the timed region, else the burst peak (a GEMM below the cap).
+    clk = clocks.summary()
+    capped = "sw_power_cap" in (clk.get("reasons") or [])
+    bf16_key = "bf16_tflops_sustained" if capped else "bf16_tflops"
     if dt == "bf16":
-        peak_tf, peak_name = peaks["bf16_tflops_sustained"], f"bf16_tflops_sustained ({peak_src})"
+        peak_tf, peak_name = peaks[bf16_key], f"{bf16_key} ({peak_src})"
     elif dt == "tf32x3":
-        peak_tf = peaks["bf16_tflops_sustained"] * 0.5
-        peak_name = (f"tf32 dense = bf16_tflops_sustained ({peak_src}) x nominal tf32/bf16 "
-                     "ratio 0.5")
+        peak_tf = peaks[bf16_key] * 0.5
+        peak_name = f"tf32 dense = {bf16_key} ({peak_src}) x nominal tf32/bf16 ratio 0.5"
     else:
         # exact fp32 runs on the FFMA units: 152 SMs x 128 fp32 lanes x 2 FLOP x max SM clock
         mhz = peaks.get("sm_max_mhz", 2070.0)
@@ -396,7 +400,6 @@ def main():
                 "avg_launch_ms": t_kernel / n_launch,
                 "peak_source": peak_name,
                 "per_kernel_ms_per_step": {k: v[1] / args.steps for k, v in sorted(agg.items())}}
-    clk = clocks.summary()
     if dt != "f32" and clk.get("sm_mhz") and clk.get("samples", 0) >= 10:
         # Context for the fraction above: the dense tensor rate per SM and clock (8192 bf16 or
         # 4096 tf32 FLOP per cycle, the per-SM rate behind the nominal 2.25 / 1.1 PFLOP/s) at the
