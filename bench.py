@@ -71,7 +71,7 @@ KERNEL_SOURCES = ("memory_bounded_linear_gb300/csrc/lce_tc.cu",
                   "memory_bounded_linear_gb300/csrc/ptx.cuh",
                   "memory_bounded_linear_gb300/csrc/lce_internal.h",
                   "memory_bounded_linear_gb300/csrc/lce_api.cu")  # launch structure
-KERNEL_SOURCE_SHA256 = "42b62af6b774a3fcd0d6017a312df42b59d684cdbc3ab0490fc6569bc08349fe"
+KERNEL_SOURCE_SHA256 = "1ca1c5777378fa11d1a0dd6914a66ee8e94341ca7b7f942579f4b60d4d258e2a"
 MEASURED_TRAFFIC = {
     # N=32768 d=6144 V=151552, strip 16384: the timed step's 21 launches -- the forward over the
     # whole vocabulary, then per strip the gradient launch and the dW + dH launch (averaged

@@ -34,8 +34,9 @@
  *     flag in the workspace header that lce_check_error turns into a status.  Rows with such a
  *     label are left out of the loss, of n_valid and of the gradients.  No call aborts the
  *     process or traps the device.
- *   - Shape rules (LCE_ERR_UNSUPPORTED_SHAPE otherwise): N >= 0, V >= 1, d >= 8 with
- *     d % 8 == 0, strip_V >= 128 with strip_V % 128 == 0, N, d, V, strip_V < 2^31.
+ *   - Shape rules (LCE_ERR_UNSUPPORTED_SHAPE otherwise): N >= 0, V >= 1, d >= 1 with a row of
+ *     d elements a multiple of 16 bytes (d % 8 == 0 for LCE_BF16, d % 4 == 0 for LCE_F32 and
+ *     LCE_F32_TF32X3), strip_V >= 128 with strip_V % 128 == 0, N, d, V, strip_V < 2^31.
  *   - Determinism: for a fixed device, shape and strip_V, every output is bitwise identical from
  *     run to run (no atomics take part in any sum; every reduction has a fixed order).
  *   - Not thread-safe across host threads only for the tracing calls (lce_trace_*).

@@ -41,17 +41,20 @@ struct Layout {
   size_t total;
 };
 
-bool shape_ok(int64_t N, int64_t d, int64_t V, int64_t strip_V) {
+// Rows of H and W are d elements: d x (element size) must be a multiple of 16 bytes (TMA row
+// strides, 16-byte vector accesses), so d % 8 == 0 for bf16 and d % 4 == 0 for fp32.
+bool shape_ok(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dt) {
+  const int64_t d_mult = (dt == LCE_BF16) ? 8 : 4;
   if (N < 0 || N > kMaxDim) return false;
   if (V < 1 || V > kMaxDim) return false;
-  if (d < 8 || d % 8 != 0 || d > kMaxDim) return false;
+  if (d < d_mult || d % d_mult != 0 || d > kMaxDim) return false;
   if (strip_V < 128 || strip_V % 128 != 0 || strip_V > kMaxDim) return false;
   return true;
 }
 
 bool make_layout(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dt, Layout* L) {
-  if (!shape_ok(N, d, V, strip_V)) return false;
   if (dt != LCE_BF16 && dt != LCE_F32 && dt != LCE_F32_TF32X3) return false;
+  if (!shape_ok(N, d, V, strip_V, dt)) return false;
   const bool x3 = (dt == LCE_F32_TF32X3);
   *L = Layout{};
   L->bn = (dt == LCE_F32) ? SIMT_BN : TC_BN;

@@ -227,7 +227,7 @@ constexpr int64_t kSplitMaxBlocks = 152 * 16;
 
 cudaError_t launch_split_tf32(const float* x, float* hi, float* lo, size_t n, cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
-  if (n % 4 != 0) return cudaErrorInvalidValue;  // whole rows of d % 8 == 0 elements
+  if (n % 4 != 0) return cudaErrorInvalidValue;  // whole rows of d % 4 == 0 elements
   const size_t n4 = n / 4;
   const int threads = 256;
   const int64_t need = static_cast<int64_t>((n4 + threads - 1) / threads);

@@ -286,8 +286,8 @@ __global__ void __launch_bounds__(THREADS, LCE_SIMT_MIN_BLOCKS) simt_strip_kerne
 }  // namespace
 
 // Alignment of the float4 accesses: every operand base is 16-byte aligned (caller pointers, the
-// W strip at col0 * d with d % 8 == 0, workspace offsets), every row stride is a multiple of 4
-// elements (d % 8 == 0, ldg % 128 == 0), and float4 offsets along the contiguous dimension are
+// W strip at col0 * d with col0 % 128 == 0, workspace offsets), every row stride is a multiple of
+// 4 elements (d % 4 == 0, ldg % 128 == 0), and float4 offsets along the contiguous dimension are
 // multiples of 4.
 cudaError_t simt_strip_gemm(const StripArgs& s, cudaStream_t stream) {
   SParams p{};

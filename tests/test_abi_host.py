@@ -90,6 +90,19 @@ def test_workspace_size_rejects_bad_shapes(lib, N, d, V, s):
     assert _ws(lib, N, d, V, s) == 0
 
 
+@pytest.mark.parametrize("d,accepted", [(4, (False, True, True)), (6, (False, False, False)),
+                                        (8, (True, True, True)), (12, (False, True, True)),
+                                        (20, (False, True, True)), (1028, (False, True, True))])
+def test_hidden_size_rule_is_sixteen_bytes_a_row(lib, d, accepted):
+    """A row of d elements must be a multiple of 16 bytes: d % 8 == 0 for bf16, d % 4 == 0 for
+    both fp32 formats."""
+    p = _Buf().addr
+    for dt, ok in zip((0, 1, 2), accepted):
+        assert (_ws(lib, 100, d, 1000, 256, dt) > 0) == ok, (d, dt)
+        # the entry point agrees: an accepted shape gets as far as the workspace-size check
+        assert _fwd(lib, p, p, p, N=100, d=d, V=1000, s=256, dt=dt, wsb=100) == (3 if ok else 2)
+
+
 class _Buf:
     """Host memory that stands in for device pointers; validation fails before any access."""
 

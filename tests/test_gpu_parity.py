@@ -333,14 +333,15 @@ def test_backward_parts_empty_batch(cuda_lib, mode):
     assert dH1.shape == (0, 64)
 
 
-def _random_shapes(seed, count):
-    """Seeded random small shapes: odd token counts, hidden sizes of any multiple of 8, vocabulary
-    sizes with ragged tails, strip widths of 128..1024, both reductions."""
+def _random_shapes(seed, count, d_mult=8):
+    """Seeded random small shapes: odd token counts, hidden sizes of any multiple of d_mult (the
+    16-byte row rule: 8 for bf16, 4 for fp32), vocabulary sizes with ragged tails, strip widths of
+    128..1024, both reductions."""
     rng = np.random.default_rng(seed)
     out = []
     for _ in range(count):
         N = int(rng.integers(1, 900))
-        d = 8 * int(rng.integers(1, 48))
+        d = d_mult * int(rng.integers(1, 384 // d_mult))
         V = int(rng.integers(2, 4000))
         strip = 128 * int(rng.integers(1, 9))
         red = "sum" if rng.random() < 0.5 else "mean"
@@ -353,9 +354,19 @@ def test_random_shapes(cuda_lib, fmt, mode):
     """Eight seeded random shapes per input format, each against the oracle at its tolerances."""
     base = W2 if fmt == "bf16" else WT
     seed = 20261202 + {"bf16": 1, "f32": 2}[fmt] + (10 if mode == "tf32x3" else 0)
-    for N, d, V, strip, red in _random_shapes(seed, 8):
+    for N, d, V, strip, red in _random_shapes(seed, 8, 8 if fmt == "bf16" else 4):
         w = base.with_sizes(N=N, d=d, V=V, strip_V=strip, reduction=red)
         parity_case(w, f32_mode=mode)
+
+
+@pytest.mark.parametrize("mode", ["exact", "tf32x3"])
+@pytest.mark.parametrize("N,d,V,strip", [(37, 4, 300, 128), (129, 12, 1000, 256),
+                                         (300, 36, 777, 512), (513, 260, 1500, 1024)])
+def test_fp32_hidden_size_multiple_of_four(cuda_lib, mode, N, d, V, strip):
+    """fp32 rows need only be 16 bytes a multiple: hidden sizes that are multiples of 4 but not of
+    8, down to d = 4 (one float4 a row, a single ragged k-block on either engine)."""
+    for red in ("mean", "sum"):
+        parity_case(WT.with_sizes(N=N, d=d, V=V, strip_V=strip, reduction=red), f32_mode=mode)
 
 
 @pytest.mark.parametrize("mode", ["exact", "tf32x3"])

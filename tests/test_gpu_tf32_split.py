@@ -35,7 +35,7 @@ def _f32(ws: np.ndarray, off: int, rows: int, cols: int, ld: int) -> np.ndarray:
     return a[:, :cols]
 
 
-@pytest.mark.parametrize("N,d,V", [(130, 72, 300), (517, 256, 1000), (64, 8, 129)])
+@pytest.mark.parametrize("N,d,V", [(130, 72, 300), (517, 256, 1000), (64, 8, 129), (50, 12, 200)])
 def test_split_parts_and_transposes_are_exact(cuda_lib, N, d, V):
     w = WORKLOADS["tiny-fp32"].with_sizes(N=N, d=d, V=V, strip_V=1024)  # one strip: V <= 1024
     H, W, y = make_inputs(w, "cuda")
