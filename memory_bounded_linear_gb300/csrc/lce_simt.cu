@@ -5,12 +5,16 @@
 //   BWD_G    G = scale (softmax - onehot) into the fp32 strip workspace
 //   DH       dH (+)= G_s W_s           DW   dW_s = G_s^T H
 //
-// A register-tiled SGEMM: 256 threads, each owning an 8 x 8 block of the tile as 2 x 2 sub-blocks
-// of 4 x 4 (rows ty*4 + {0..3} and 64 + ty*4 + {0..3}, columns likewise with tx), k-blocks of 16
-// staged in shared memory as [k][m] and [k][n] rows, so every k step is two float4 reads of A and
-// two of B for 64 FFMAs.  The next k-block is loaded into registers while the current one is
-// multiplied (one barrier per k-block).  Operands are K-major or MN-major per mode; both are read
-// as float4 along their contiguous dimension, with a scalar path at the ragged edges.
+// A register-tiled SGEMM: 128 threads (four warps, each owning 32 rows x 128 columns of the
+// tile), each thread an 8 x 16 block of outputs: rows warp*32 + r*4 + {0..3} and the same + 16,
+// columns c*4 + {0..3} + 32 q for q = 0..3, with r = lane / 8 and c = lane % 8.  A row of the tile
+// therefore lives in the 8 lanes of one warp that share r.  k-blocks of 8 are staged in shared
+// memory as [k][m] and [k][n] rows, so every k step is two float4 reads of A and four of B for
+// 128 FFMAs; the reads of step k + 1 are issued before the FFMAs of step k, and the next k-block
+// is loaded into registers while the current one is multiplied (one barrier per k-block).
+// Operands are K-major or MN-major per mode; both are read as float4 along their contiguous
+// dimension, with a scalar path at the ragged edges.  Two blocks per SM, up to 255 registers a
+// thread: 128 accumulators, two sets of 24 fragment values, 16 staged operand values.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -24,12 +28,12 @@ namespace {
 
 constexpr int TM = 128;
 constexpr int TN = SIMT_BN;  // 128
-constexpr int TK = 16;
-constexpr int THREADS = 256;  // 16 x 16 threads, 8 x 8 outputs each
+constexpr int TK = 8;
+constexpr int THREADS = 128;  // 4 warps x 32 lanes, 8 x 16 outputs each
 constexpr int RASTER = 8;     // row tiles per rasterisation group
 static_assert(TN == 128, "the epilogues assume 128-column tiles");
 // Resident blocks per SM the kernel is compiled for (build-time tunable): 2 caps registers at
-// 128 per thread; 1 leaves the compiler up to 255.
+// 255 per thread.
 #ifndef LCE_SIMT_MIN_BLOCKS
 #define LCE_SIMT_MIN_BLOCKS 2
 #endif
@@ -62,30 +66,30 @@ struct SParams {
 };
 
 // Shared-memory layout of a staged operand block: [TK][128] floats, element (k, m) at column
-// m ^ swz(k).  The swizzle flips bits 3-4 of m by k / 4, so the transposed scalar stores of a
-// K-major block (8 consecutive m by 4 k-groups per warp) land in 32 distinct banks, while groups
-// of 4 consecutive m stay contiguous for the float4 reads of the multiply.
-__device__ __forceinline__ int swz(int k) { return ((k >> 2) & 3) << 3; }
+// m ^ swz(k).  The swizzle flips bit 4 of m for k = 4..7: a warp's transposed scalar stores of a
+// K-major block (16 consecutive m at k and 16 at k + 4) then land in 32 distinct banks, while
+// groups of 4 consecutive m stay contiguous for the float4 reads of the multiply.
+__device__ __forceinline__ int swz(int k) { return ((k >> 2) & 1) << 4; }
 
 // A thread's two fragments of a TK x 128 operand block, four consecutive elements each along the
-// operand's contiguous dimension.  Fragment f covers u = t + 256 f:
-//   K-major (stride 1 along k):  m = u / 4,  k = (u % 4) * 4       (fragment 1: m + 64)
-//   MN-major (stride 1 along m): k = u / 32, m = (u % 32) * 4      (fragment 1: k + 8)
+// operand's contiguous dimension.  Fragment f covers u = t + 128 f:
+//   K-major (stride 1 along k):  m = u / 2,  k = (u % 2) * 4       (fragment 1: m + 64)
+//   MN-major (stride 1 along m): k = u / 32, m = (u % 32) * 4      (fragment 1: k + 4)
 // One base pointer per operand (fragment 0 of the current k-block) advances by TK along k.
 template <bool KMAJ>
 struct Operand {
   const float* base;
   int64_t step;  // elements between consecutive k-blocks
-  int off1;      // fragment 1 relative to fragment 0 (64 rows, or 8 k-rows)
+  int off1;      // fragment 1 relative to fragment 0 (64 rows, or TK / 2 k-rows)
   int mn0, k0;   // fragment 0's m and k offsets within the block (tile-relative m added)
   unsigned ok;   // bit f: fragment f's m range lies inside the operand
 
   __device__ __forceinline__ void init(const float* X, int64_t s_mn, int64_t s_k, int tile_mn,
                                        int MN, int t) {
-    mn0 = tile_mn + (KMAJ ? t / 4 : (t % 32) * 4);
-    k0 = KMAJ ? (t % 4) * 4 : t / 32;
+    mn0 = tile_mn + (KMAJ ? t / 2 : (t % 32) * 4);
+    k0 = KMAJ ? (t % 2) * 4 : t / 32;
     base = X + static_cast<int64_t>(mn0) * s_mn + static_cast<int64_t>(k0) * s_k;
-    off1 = KMAJ ? static_cast<int>(64 * s_mn) : static_cast<int>(8 * s_k);
+    off1 = KMAJ ? static_cast<int>(64 * s_mn) : static_cast<int>((TK / 2) * s_k);
     step = static_cast<int64_t>(TK) * s_k;
     ok = KMAJ ? ((mn0 < MN ? 1u : 0u) | (mn0 + 64 < MN ? 2u : 0u))
               : (mn0 + 3 < MN ? 3u : 0u);
@@ -102,7 +106,7 @@ struct Operand {
         v[f][0] = q.x; v[f][1] = q.y; v[f][2] = q.z; v[f][3] = q.w;
       } else {
         const int mn = mn0 + ((KMAJ && f) ? 64 : 0);
-        const int k = kb * TK + k0 + ((!KMAJ && f) ? 8 : 0);
+        const int k = kb * TK + k0 + ((!KMAJ && f) ? TK / 2 : 0);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const bool in = KMAJ ? (mn < MN && k + i < K) : (k < K && mn + i < MN);
@@ -116,16 +120,17 @@ struct Operand {
 #pragma unroll
     for (int f = 0; f < 2; ++f) {
       if (KMAJ) {
-        const int m = t / 4 + 64 * f, k = (t % 4) * 4;
+        const int m = t / 2 + 64 * f, k = (t % 2) * 4;
 #pragma unroll
         for (int i = 0; i < 4; ++i) S[k + i][m ^ swz(k + i)] = v[f][i];
       } else {
-        const int k = t / 32 + 8 * f, m = (t % 32) * 4;
+        const int k = t / 32 + (TK / 2) * f, m = (t % 32) * 4;
         *reinterpret_cast<float4*>(&S[k][m ^ swz(k)]) =
             make_float4(v[f][0], v[f][1], v[f][2], v[f][3]);
       }
     }
   }
+
 };
 
 // Grouped rasterisation: RASTER row tiles sweep the column tiles together (operand reuse in L2).
@@ -139,6 +144,24 @@ __device__ __forceinline__ void tile_of(int t, int tiles_m, int tiles_n, int& tm
   tn = r / gm;
 }
 
+// One k step's fragments from staged block `buf`: a = rows arow + {0..3}, arow + 16 + {0..3};
+// b = columns bcol + 32 q + {0..3}, q = 0..3, as pairs of adjacent columns (element (k, m) at
+// column m ^ swz(k)).
+__device__ __forceinline__ void fragments(const float (*As)[TM], const float (*Bs)[TN], int kk,
+                                          int arow, int bcol, float (&a)[8], float2 (&b)[8]) {
+  const int z = swz(kk);
+  const float4 a0 = *reinterpret_cast<const float4*>(&As[kk][arow ^ z]);
+  const float4 a1 = *reinterpret_cast<const float4*>(&As[kk][(arow + 16) ^ z]);
+  a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+  a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = *reinterpret_cast<const float4*>(&Bs[kk][(bcol + 32 * q) ^ z]);
+    b[2 * q] = make_float2(v.x, v.y);
+    b[2 * q + 1] = make_float2(v.z, v.w);
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, LCE_SIMT_MIN_BLOCKS) simt_strip_kernel(const SParams p) {
   __shared__ __align__(16) float As[2][TK][TM];
@@ -147,14 +170,18 @@ __global__ void __launch_bounds__(THREADS, LCE_SIMT_MIN_BLOCKS) simt_strip_kerne
   int tm, tn;
   tile_of(blockIdx.x, p.tiles_m, p.tiles_n, tm, tn);
   const int t = threadIdx.x;
-  const int tx = t & 15, ty = t >> 4;
+  const int warp = t >> 5, lane = t & 31;
+  const int r = lane >> 3, c = lane & 7;  // the 8 lanes sharing r hold one row's 128 columns
+  const int arow = warp * 32 + r * 4, bcol = c * 4;
   const int m0 = tm * TM, n0 = tn * TN;
 
-  float acc[8][8];
+  // acc2[i][p]: outputs (row i, columns 2p and 2p + 1) of the thread's 8 x 16, updated two at a
+  // time by the packed fp32 FMA (each lane an ordinary round-to-nearest fp32 FMA)
+  float2 acc2[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 8; ++j) acc2[i][j] = make_float2(0.f, 0.f);
 
   // operand majorness per mode: A = H (K-major) or G (K-major for dH, MN-major for dW);
   // B = W strip (K-major for the logits, MN-major for dH) or H (MN-major for dW)
@@ -179,19 +206,19 @@ __global__ void __launch_bounds__(THREADS, LCE_SIMT_MIN_BLOCKS) simt_strip_kerne
       oa.load(kb + 1, kfull, p.M, p.K, va);
       ob.load(kb + 1, kfull, p.Ncols, p.K, vb);
     }
+    float a[2][8];
+    float2 b[2][8];
+    fragments(As[cur], Bs[cur], 0, arow, bcol, a[0], b[0]);
 #pragma unroll
     for (int kk = 0; kk < TK; ++kk) {
-      const int z = swz(kk);
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][kk][(ty * 4) ^ z]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][kk][(64 + ty * 4) ^ z]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][kk][(tx * 4) ^ z]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][kk][(64 + tx * 4) ^ z]);
-      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      if (kk + 1 < TK)  // step kk + 1's reads in flight during step kk's FMAs
+        fragments(As[cur], Bs[cur], kk + 1, arow, bcol, a[(kk + 1) & 1], b[(kk + 1) & 1]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i) {
+        const float2 ai = make_float2(a[kk & 1][i], a[kk & 1][i]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc2[i][j] = __ffma2_rn(ai, b[kk & 1][j], acc2[i][j]);
+      }
     }
     if (more) {  // the other buffer was last read before the previous barrier
       oa.store(As[cur ^ 1], va, t);
@@ -200,35 +227,43 @@ __global__ void __launch_bounds__(THREADS, LCE_SIMT_MIN_BLOCKS) simt_strip_kerne
     __syncthreads();
   }
 
-  // this thread's rows and columns (tile-local): r(i) = (i / 4) * 64 + ty * 4 + i % 4, same for c
-  auto row_of = [&](int i) { return (i >> 2) * 64 + ty * 4 + (i & 3); };
-  auto col_of = [&](int j) { return (j >> 2) * 64 + tx * 4 + (j & 3); };
+  // this thread's rows and columns (tile-local), and output (i, j) of its 8 x 16
+  auto row_of = [&](int i) { return arow + (i >> 2) * 16 + (i & 3); };
+  auto col_of = [&](int j) { return bcol + (j >> 2) * 32 + (j & 3); };
+  float acc[8][16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      acc[i][2 * j] = acc2[i][j].x;
+      acc[i][2 * j + 1] = acc2[i][j].y;
+    }
 
   if (MODE == MODE_FWD_LSE) {
-    // The 16 threads sharing a row (tx = 0..15) are one half-warp: reduce over them by shuffles.
+    // The 8 lanes sharing a row (c = 0..7) are consecutive: reduce over them by shuffles.
     const int ncols = min(TN, p.strip_cols - n0);  // >= 1
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int row = m0 + row_of(i);
       float mx = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 16; ++j)
         if (col_of(j) < ncols) mx = fmaxf(mx, acc[i][j]);
 #pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      for (int o = 4; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       float sm = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 16; ++j)
         if (col_of(j) < ncols) sm += expf(acc[i][j] - mx);
 #pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      for (int o = 4; o >= 1; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
       if (row < p.M) {
-        if (tx == 0) p.part[static_cast<size_t>(tn) * p.M + row] = make_float2(mx, sm);
+        if (c == 0) p.part[static_cast<size_t>(tn) * p.M + row] = make_float2(mx, sm);
         const int64_t y = p.labels[row];
         const int64_t rel = y - static_cast<int64_t>(p.col0 + n0);
         if (y != p.ignore_index && y >= 0 && y < p.V && rel >= 0 && rel < ncols) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
+          for (int j = 0; j < 16; ++j)
             if (col_of(j) == rel) p.tgt[row] = acc[i][j];
         }
       }
@@ -242,11 +277,11 @@ __global__ void __launch_bounds__(THREADS, LCE_SIMT_MIN_BLOCKS) simt_strip_kerne
       if (row >= p.M) continue;
       const int64_t y = p.labels[row];
       const bool ok = (y != p.ignore_index) && (y >= 0) && (y < p.V);
-      if (!ok && y != p.ignore_index && p.first_strip && tn == 0 && tx == 0)
+      if (!ok && y != p.ignore_index && p.first_strip && tn == 0 && c == 0)
         atomicOr(p.err, ERR_LABEL);
       const float l = ok ? p.lse[row] : 0.f;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < 4; ++h) {
         float g[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -267,17 +302,17 @@ __global__ void __launch_bounds__(THREADS, LCE_SIMT_MIN_BLOCKS) simt_strip_kerne
       const int row = m0 + row_of(i);
       if (row >= p.c_rows) continue;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < 4; ++h) {
         const int col = n0 + col_of(h * 4);
         if (col >= p.c_cols) continue;  // c_cols % 4 == 0: a group is all in or all out
-        float4* c = reinterpret_cast<float4*>(p.C + static_cast<size_t>(row) * p.ldc + col);
+        float4* cp = reinterpret_cast<float4*>(p.C + static_cast<size_t>(row) * p.ldc + col);
         float4 v = make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2],
                                acc[i][h * 4 + 3]);
         if (p.accumulate) {
-          const float4 o = *c;
+          const float4 o = *cp;
           v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
         }
-        *c = v;
+        *cp = v;
       }
     }
   }
@@ -315,7 +350,7 @@ cudaError_t simt_strip_gemm(const StripArgs& s, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   if (p.M == 0 || p.Ncols == 0 || p.K == 0) return cudaSuccess;
-  // 32-bit index arithmetic in the kernel: fragment offsets of 64 rows (or 16 k-rows) of the
+  // 32-bit index arithmetic in the kernel: fragment offsets of 64 rows (or 4 k-rows) of the
   // largest stride, and tile-relative indices up to M + 255, N + 255, K + 31
   const int64_t max_stride = std::max(std::max(p.a_sm, p.a_sk), std::max(p.b_sn, p.b_sk));
   const int64_t kIntMax = 0x7fffffffLL;
