@@ -10,8 +10,9 @@
 // columns c*4 + {0..3} + 32 q for q = 0..3, with r = lane / 8 and c = lane % 8.  A row of the tile
 // therefore lives in the 8 lanes of one warp that share r.  k-blocks of 8 are staged in shared
 // memory as [k][m] and [k][n] rows, so every k step is two float4 reads of A and four of B for
-// 128 FFMAs; the reads of step k + 1 are issued before the FFMAs of step k, and the next k-block
-// is loaded into registers while the current one is multiplied (one barrier per k-block).
+// 128 FMAs, issued as 64 packed fp32 FMAs (__ffma2_rn) on pairs of adjacent columns with a
+// broadcast A value; the reads of step k + 1 are issued before the FMAs of step k, and the next
+// k-block is loaded into registers while the current one is multiplied (one barrier per k-block).
 // Operands are K-major or MN-major per mode; both are read as float4 along their contiguous
 // dimension, with a scalar path at the ragged edges.  Two blocks per SM, up to 255 registers a
 // thread: 128 accumulators, two sets of 24 fragment values, 16 staged operand values.
