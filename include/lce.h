@@ -156,12 +156,12 @@ lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* lab
  * point: it is an addition of this library, with no counterpart in the papers.
  *
  * Some callers may not call cudaMalloc at all: a plugin of an engine that owns all device memory
- * through its own pool and only lends out the buffers it planned; code enqueuing work while its
- * stream is being captured into a CUDA graph; latency-critical code that cannot take the device
- * synchronisation an allocation may bring.  This entry point computes exactly what lce_forward
- * computes (same kernels, same results) but takes its workspace from a fixed array of
- * LCE_STATIC_SCRATCH_BYTES (16 MiB) that the library keeps in device memory; it allocates nothing
- * and frees nothing.  The caller still passes the inputs and the outputs (loss, lse, n_valid as
+ * through its own pool and only lends out the buffers it planned; a service whose device memory
+ * budget is fixed at start-up and may not grow per request; latency-critical code that cannot
+ * take the cost of an allocation or the device-wide synchronisation of a free.  This entry point
+ * computes exactly what lce_forward computes (same kernels, same results) but takes its workspace
+ * from a fixed array of LCE_STATIC_SCRATCH_BYTES (16 MiB) that the library keeps in device
+ * memory; it allocates nothing and frees nothing.  The caller still passes the inputs and the outputs (loss, lse, n_valid as
  * in lce_forward).
  *   - Size limit: when lce_workspace_size(N, d, V, strip_V, dtype) exceeds
  *     LCE_STATIC_SCRATCH_BYTES the call returns LCE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing

@@ -108,6 +108,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 thread_local char g_last_error[384] = "none";
 thread_local bool g_detail_set = false;
 
+int g_sms[kMaxDevices];
+signed char g_dev_ok[kMaxDevices];  // 0 unknown, 1 ok, -1 not sm_103
+
+}  // namespace
+
 // Records the CUDA error of a failed call unless the failing step already described itself.
 cudaError_t note(cudaError_t e) {
   if (e != cudaSuccess && !g_detail_set)
@@ -116,13 +121,10 @@ cudaError_t note(cudaError_t e) {
   return e;
 }
 
-int g_sms[64];
-signed char g_dev_ok[64];  // 0 unknown, 1 ok, -1 not sm_103
-
 lce_status_t check_device(int* num_sms) {
   int dev = 0;
   if (note(cudaGetDevice(&dev)) != cudaSuccess) return LCE_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return LCE_ERR_UNSUPPORTED_DEVICE;
+  if (dev < 0 || dev >= kMaxDevices) return LCE_ERR_UNSUPPORTED_DEVICE;
   // Make the device's primary context current on this thread: the tensor maps are encoded with
   // the driver API, which needs a current context, and a fresh thread (e.g. autograd's backward
   // worker) has none until its first context-creating runtime call.
@@ -140,6 +142,8 @@ lce_status_t check_device(int* num_sms) {
   *num_sms = g_sms[dev];
   return LCE_OK;
 }
+
+namespace {
 
 // --------------------------------------------------------------------------- launch bookkeeping
 std::atomic<int64_t> g_launches{0};

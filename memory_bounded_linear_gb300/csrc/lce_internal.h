@@ -4,7 +4,20 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "lce.h"
+
 namespace lce {
+
+// Devices a process may use with this library (ordinals 0 .. kMaxDevices-1).
+constexpr int kMaxDevices = 64;
+
+// Checks that the current device is compute capability 10.3 and makes its primary context
+// current on the calling thread; fills the device's SM count.  LCE_OK, LCE_ERR_CUDA or
+// LCE_ERR_UNSUPPORTED_DEVICE (lce_api.cu).
+lce_status_t check_device(int* num_sms);
+// Passes a CUDA status through, recording the name of a failure for lce_last_cuda_error unless
+// the failing step already described itself (lce_api.cu).
+cudaError_t note(cudaError_t e);
 
 // Error-flag bits kept in the first word of the workspace header.
 constexpr unsigned ERR_LABEL = 1u;     // a label outside [0, V) that is not ignore_index

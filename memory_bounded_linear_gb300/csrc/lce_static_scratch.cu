@@ -3,38 +3,42 @@
 //
 // Who needs it: code that is handed a stream but may not allocate device memory itself -- a
 // plugin inside an inference or training engine that owns every byte of device memory through
-// its own pool and only lends its plugins the buffers it planned; code that runs while a stream
-// is being captured into a CUDA graph, where cudaMalloc is not allowed on the capturing stream
-// (and cudaFree would synchronise the device); latency-critical paths that cannot afford the
-// device-wide synchronisation a cudaMalloc/cudaFree pair may imply.  Such a caller still passes
-// its inputs and outputs; only the scratch comes from here.
+// its own pool and only lends its plugins the buffers it planned; a service that fixes its device
+// memory budget at start-up and must not grow it per request; latency-critical paths that cannot
+// take the cost of cudaMalloc or the device-wide synchronisation of a cudaFree.  Such a caller
+// still passes its inputs and outputs; only the scratch comes from here.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <atomic>
 
 #include "lce.h"
+#include "lce_internal.h"
 
 namespace {
 
 // The scratch array.  Every GPU that loads this library holds these bytes until the process exits.
 __device__ __align__(256) unsigned char g_static_scratch[LCE_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+std::atomic<void*> g_scratch_addr[lce::kMaxDevices];
 
 // Device address of the array on the current device.  In host code the array's name is only a
 // host-side handle, so the address is asked from the runtime, once per device, with that device
-// current.
+// current.  The device is checked first: a device of another architecture has no image of this
+// library, so it is refused as unsupported rather than failing the lookup.
 lce_status_t scratch_address(void** out) {
+  int num_sms = 0;
+  lce_status_t st = lce::check_device(&num_sms);  // also makes the device's context current
+  if (st != LCE_OK) return st;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LCE_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return LCE_ERR_UNSUPPORTED_DEVICE;
+  if (lce::note(cudaGetDevice(&dev)) != cudaSuccess) return LCE_ERR_CUDA;
   void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
   if (p == nullptr) {
-    if (cudaSetDevice(dev) != cudaSuccess) return LCE_ERR_CUDA;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+    if (lce::note(cudaGetSymbolAddress(&p, g_static_scratch)) != cudaSuccess) return LCE_ERR_CUDA;
+    if (p == nullptr) {
+      lce::set_error_detail("no device address for the static scratch array");
       return LCE_ERR_CUDA;
+    }
     g_scratch_addr[dev].store(p, std::memory_order_release);
   }
   *out = p;
@@ -59,8 +63,9 @@ extern "C" lce_status_t lce_forward_static_scratch(
                    n_valid, scratch, LCE_STATIC_SCRATCH_BYTES, stream);
   if (st != LCE_OK) return st;
   if (device_error_flags != nullptr &&
-      cudaMemcpyAsync(device_error_flags, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice,
-                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      lce::note(cudaMemcpyAsync(device_error_flags, scratch, sizeof(uint32_t),
+                                cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream))) !=
+          cudaSuccess)
     return LCE_ERR_CUDA;
   return LCE_OK;
 }

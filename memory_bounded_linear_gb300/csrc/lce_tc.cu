@@ -632,10 +632,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (tloc >= 0) p.tgt[row] = t;
           }
         } else {
-          // MODE_BWD_G: G = scale * (exp(Z - lse) - onehot) -> strip workspace
+          // MODE_BWD_G: G = scale * (exp(Z - lse) - onehot) -> strip workspace.  Rows that are
+          // not valid (ignored, bad label, past N) get exact zeros by selection, never as
+          // 0 * exp(Z): their logits are not bounded by an lse of theirs, so exp can overflow
+          // to inf there (Z above about 88.7), and 0 * inf would be NaN.
           if (row_ok && !label_ok && y != p.ignore_index && jb.first_strip && tp.tn == 0)
             atomicOr(p.err, ERR_LABEL);
-          const float scale = label_ok ? scale_valid : 0.f;
+          const float scale = scale_valid;
           const float nl = label_ok ? -p.lse[row] * LOG2E : 0.f;
           if (!wait_bar(tfull, aph, abort_flag, p.err)) break;
           ptx::tc_fence_after();
@@ -652,7 +655,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               if (c * 32 < ncols) {
                 float v[32];
                 ptx::tmem_load32(tbase + c * 32, v);
-                const int lim = ncols - c * 32;
+                const int lim = label_ok ? ncols - c * 32 : 0;  // no live column on such rows
                 const int jt = tloc - c * 32;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -725,7 +728,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (c * 32 < ncols) {
               float v[32];
               ptx::tmem_load32(tbase + c * 32, v);
-              const int lim = ncols - c * 32;
+              const int lim = label_ok ? ncols - c * 32 : 0;  // no live column on such rows
               const int jt = tloc - c * 32;
 #pragma unroll
               for (int j = 0; j < 32; j += 2) {
