@@ -411,65 +411,103 @@ def main():
         roofline["peak_at_sampled_clock"] = p_clk
         roofline["frac_at_sampled_clock"] = achieved / p_clk
 
-    # End to end through the public API: every step copies its inputs (H, W, labels) from pinned
-    # host memory to the device, runs forward+backward and reads the loss back to the host.  The
-    # copies run on their own stream into one of two device input buffers, so step i+1's copy
-    # overlaps step i's compute (a training loop prefetching its next batch).
-    e2e = None
+    # End to end through the public API, two variants, each pipelined over K steps.
+    #  * e2e (every result back): each step copies its inputs (H, W, labels) from pinned host memory
+    #    to the device, runs forward+backward, and copies EVERY output of the call (loss, lse, dH,
+    #    dW) back to pinned host memory -- the library used as a host-to-host operator.
+    #  * e2e_loss_only (the training-loop figure): the same input copies, but only the loss comes
+    #    back; dH and dW stay on the device, where the previous layer's backward and the optimizer
+    #    use them.
+    # Three streams: inputs of step i+1 are copied in while step i computes and step i-1's results
+    # are copied out; device input and output buffers are double-buffered.
+    e2e = e2e_loss = None
     if not args.no_e2e:
         Hh = H.cpu().pin_memory()
         Wh = W.cpu().pin_memory()
         yh = y.cpu().pin_memory()
-        loss_h = torch.empty((2,), dtype=torch.float32).pin_memory()
+        in_bytes = sum(t.numel() * t.element_size() for t in (Hh, Wh, yh))
         bufs = [(torch.empty_like(H), torch.empty_like(W), torch.empty_like(y)) for _ in range(2)]
-        copy_stream = torch.cuda.Stream(dev)
+        outs = [(torch.empty((), device=dev), torch.empty(N, device=dev),
+                 torch.empty((), dtype=torch.int64, device=dev), torch.empty(N, d, device=dev),
+                 torch.empty(V, d, device=dev)) for _ in range(2)]
+        host_out = (torch.empty((), dtype=torch.float32).pin_memory(),
+                    torch.empty(N, dtype=torch.float32).pin_memory(),
+                    torch.empty(N, d, dtype=torch.float32).pin_memory(),
+                    torch.empty(V, d, dtype=torch.float32).pin_memory())
+        copy_in_stream = torch.cuda.Stream(dev)
+        copy_out_stream = torch.cuda.Stream(dev)
         copied = [torch.cuda.Event() for _ in range(2)]
         consumed = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        drained = [torch.cuda.Event() for _ in range(2)]
 
         def copy_in(i):
             b = i % 2
-            with torch.cuda.stream(copy_stream):
+            with torch.cuda.stream(copy_in_stream):
                 if i >= 2:
-                    copy_stream.wait_event(consumed[b])  # step i-2 is done with this buffer
+                    copy_in_stream.wait_event(consumed[b])  # step i-2 is done with this buffer
                 for dst, src in zip(bufs[b], (Hh, Wh, yh)):
                     dst.copy_(src, non_blocking=True)
-                copied[b].record(copy_stream)
+                copied[b].record(copy_in_stream)
 
-        def compute(i):
+        def compute(i, results_back):
             b = i % 2
             stream.wait_event(copied[b])
+            if i >= 2 and results_back:
+                stream.wait_event(drained[b])  # step i-2's results have left this buffer
             Hd, Wd, yd = bufs[b]
+            lo, ls, n_v, dHo, dWo = outs[b]
             api.lce_forward(Hd, Wd, yd, strip_V=S, reduction=w.reduction, workspace=ws,
-                            out=(loss, lse, nv), stream=stream, f32_mode=fm)
-            api.lce_backward(Hd, Wd, yd, lse, nv, one, strip_V=S, reduction=w.reduction,
-                             workspace=ws, dH=dH, dW=dW, stream=stream, f32_mode=fm)
+                            out=(lo, ls, n_v), stream=stream, f32_mode=fm)
+            api.lce_backward(Hd, Wd, yd, ls, n_v, one, strip_V=S, reduction=w.reduction,
+                             workspace=ws, dH=dHo, dW=dWo, stream=stream, f32_mode=fm)
             consumed[b].record(stream)
-            loss_h[b].copy_(loss, non_blocking=True)
+            if not results_back:
+                host_out[0].copy_(lo, non_blocking=True)
+                return
+            computed[b].record(stream)
+            with torch.cuda.stream(copy_out_stream):
+                copy_out_stream.wait_event(computed[b])
+                for dst, src in zip(host_out, (lo, ls, dHo, dWo)):
+                    dst.copy_(src, non_blocking=True)
+                drained[b].record(copy_out_stream)
 
-        def pipeline(k):
-            copy_stream.wait_stream(stream)
+        def pipeline(k, results_back):
+            copy_in_stream.wait_stream(stream)
+            copy_out_stream.wait_stream(stream)
             copy_in(0)
             for i in range(k):
                 if i + 1 < k:
                     copy_in(i + 1)
-                compute(i)
+                compute(i, results_back)
+            stream.wait_stream(copy_out_stream)  # the last results have reached the host
 
-        pipeline(2)
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        k2 = max(3, args.steps)  # the first step's copy is not overlapped: amortise it over K
-        e0.record(stream)
-        pipeline(k2)
-        e1.record(stream)
-        barrier()
-        e_ms = max_over_ranks(e0.elapsed_time(e1) / k2, world, dev)
+        def time_e2e(results_back):
+            pipeline(2, results_back)
+            barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            k2 = max(3, args.steps)  # the first step's copy is not overlapped: amortise it over K
+            e0.record(stream)
+            pipeline(k2, results_back)
+            e1.record(stream)
+            barrier()
+            return max_over_ranks(e0.elapsed_time(e1) / k2, world, dev)
+
+        e_ms = time_e2e(True)
+        out_bytes = sum(t.numel() * t.element_size() for t in host_out)
         e2e = {"value": tokens_per_second(world, N, e_ms), "unit": "tokens/s",
-               "h2d_bytes_per_step": (Hh.numel() * Hh.element_size() + Wh.numel() * Wh.element_size()
-                                      + yh.numel() * yh.element_size()),
-               "d2h_bytes_per_step": 4, "ms_per_step": e_ms,
-               "overlap": "inputs of step i+1 copied on a second stream during step i"}
-        del bufs
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+               "ms_per_step": e_ms,
+               "results": "loss, lse, dH and dW copied back to pinned host memory every step",
+               "overlap": "inputs of step i+1 copied in and results of step i-1 copied out "
+                          "during step i"}
+        l_ms = time_e2e(False)
+        e2e_loss = {"value": tokens_per_second(world, N, l_ms), "unit": "tokens/s",
+                    "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4, "ms_per_step": l_ms,
+                    "results": "loss only; dH and dW stay on the device (training-loop figure)",
+                    "overlap": "inputs of step i+1 copied in during step i"}
+        del bufs, outs, host_out
 
     # Delayed weight gradient (lce_backward_parts): the dgrad-only and wgrad-only backward calls
     # against the fused backward on the same inputs and workspace, CUDA events on the launching
@@ -558,6 +596,7 @@ def main():
             "roofline": roofline,
             "clocks": clk,
             "e2e": e2e,
+            "e2e_loss_only": e2e_loss,
             "delayed_wgrad": delayed_wgrad,
             "cuda_graph": cuda_graph,
             "cpu_baseline": cpu,

@@ -216,7 +216,10 @@ __device__ __forceinline__ TilePos locate(const KParams& p, int t) {
 // counter -- tiles come out in job and raster order, so the tiles in flight at any moment stay
 // together however unevenly the SMs progress, and operands keep being shared through L2 -- and
 // posts each ticket into the ring `tq` of both CTAs of a pair.  Every other role reads the
-// tickets from its own CTA's ring and hands the slot back.  -1 ends the sequence.
+// tickets from its own CTA's ring and hands the slot back.  -1 ends the sequence.  The producer
+// takes the ticket of its next tile from the counter as soon as it has posted the current one, so
+// the atomic's round trip overlaps the current tile's loads instead of opening a gap in the
+// operand stream at every tile boundary.
 template <bool PAIR>
 struct TileQueue {
   Ctl* ctl;
@@ -229,13 +232,13 @@ struct TileQueue {
     if (++slot == TQ) { slot = 0; ph ^= 1u; }
   }
 
-  // Scheduler: the next ticket, posted to both CTAs.  Returns -1 at the end (and after a
-  // timeout); the last unit to finish clears the counters for the next launch.
-  __device__ __forceinline__ int post(unsigned* sched, int num_tiles, int units) {
+  // Scheduler: posts `ticket` (taken from the counter sched[0] beforehand) to both CTAs, or -1
+  // when it is past the last tile.  Returns what was posted (-1 also after a timeout); the last
+  // unit to receive -1 clears the counters for the next launch.
+  __device__ __forceinline__ int post(unsigned ticket, unsigned* sched, int num_tiles, int units) {
     const uint32_t empty = ptx::smem_addr(&ctl->tq_empty[slot]);
     if (!wait_bar<PAIR>(empty, ph ^ 1u, abort_flag, err)) return -1;
-    int t = static_cast<int>(atomicAdd(&sched[0], 1u));
-    if (t >= num_tiles) t = -1;
+    const int t = (ticket < static_cast<unsigned>(num_tiles)) ? static_cast<int>(ticket) : -1;
     ctl->tq[slot] = t;
     const uint32_t full = ptx::smem_addr(&ctl->tq_full[slot]);
     if (PAIR) {
@@ -294,19 +297,24 @@ __host__ __device__ constexpr bool b_mn_major() {
   return (MODE == MODE_DH || MODE == MODE_DW) && OP == OP_BF16;
 }
 
-// The kernel is compiled per set of modes it may meet (a bit mask of MODE_*): the forward kernel
-// carries only the forward epilogue, the backward kernel the three backward ones.  Keeping the
-// code of each kernel small matters: a kernel carrying all four epilogues ran 13% slower.
+// The kernel is compiled per set of modes a launch carries (a bit mask of MODE_*): the forward;
+// the gradient; dW and dH; and all three backward modes (the launches that overlap dW and dH of
+// one strip with the next strip's gradient).  Keeping the code of each kernel small matters: a
+// kernel carrying all four epilogues ran 13% slower, and the dW + dH launches of the kernel
+// carrying all three backward modes ran slower than they do alone.
 constexpr int MODES_FWD = 1 << MODE_FWD_LSE;
-constexpr int MODES_BWD = (1 << MODE_BWD_G) | (1 << MODE_DH) | (1 << MODE_DW);
+constexpr int MODES_G = 1 << MODE_BWD_G;
+constexpr int MODES_DHDW = (1 << MODE_DH) | (1 << MODE_DW);
+constexpr int MODES_BWD = MODES_G | MODES_DHDW;
 template <int MODES>
-__device__ __forceinline__ constexpr bool has_mode(int m) {
+__host__ __device__ __forceinline__ constexpr bool has_mode(int m) {
   return ((MODES >> m) & 1) != 0;
 }
 // The job's mode as the compiler sees it: a constant when the kernel serves a single mode.
 template <int MODES>
 __device__ __forceinline__ int mode_of(const Job& jb) {
   if constexpr (MODES == MODES_FWD) return MODE_FWD_LSE;
+  else if constexpr (MODES == MODES_G) return MODE_BWD_G;
   else return jb.mode;
 }
 
@@ -331,16 +339,19 @@ struct Ring {
 };
 
 // Producer side of one tile: its k-blocks of A and B (every operand part) into the stage ring.
-// False when a wait gave up.  `withhold_first` is the timeout-path test hook.
+// False when a wait gave up.  `withhold_first` is the timeout-path test hook.  The job's fields
+// come in as scalars, read once per tile: this one thread's time per k-block paces the operand
+// stream, and the TMA instructions' memory clobbers would make it re-read fields of the job in
+// every k-block.
 template <int MODE, bool PAIR, int OP>
-__device__ __forceinline__ bool produce_tile(const Job& jb, const CUtensorMap* mA,
-                                             const CUtensorMap* mB, int m0, int n0, uint32_t base,
-                                             Ctl* ctl, Ring& r, volatile int* abort_flag,
-                                             unsigned* err, uint32_t rank, bool withhold_first) {
+__device__ __forceinline__ bool produce_tile(int nkb, int b_off, const CUtensorMap* mA, const CUtensorMap* mB, int m0,
+                                             int n0, uint32_t base, Ctl* ctl, Ring& r,
+                                             volatile int* abort_flag, unsigned* err,
+                                             uint32_t rank, bool withhold_first) {
   using Cf = Cfg<PAIR, OP>;
   constexpr bool A_MN = a_mn_major<MODE, OP>();
   constexpr bool B_MN = b_mn_major<MODE, OP>();
-  for (int kb = 0; kb < jb.nkb; ++kb) {
+  for (int kb = 0; kb < nkb; ++kb) {
     const uint32_t empty = ptx::smem_addr(&ctl->empty[r.stage]);
     const uint32_t full_local = ptx::smem_addr(&ctl->full[r.stage]);
     if (!wait_bar(empty, r.ph ^ 1u, abort_flag, err)) return false;
@@ -365,12 +376,12 @@ __device__ __forceinline__ bool produce_tile(const Job& jb, const CUtensorMap* m
           load(sa, &mA[part], kb * Cf::BK, m0);
         }
         if (B_MN) {
-          const int krow = (MODE == MODE_DH ? jb.b_off : 0) + kb * Cf::BK;
+          const int krow = (MODE == MODE_DH ? b_off : 0) + kb * Cf::BK;
 #pragma unroll
           for (int c = 0; c < Cf::B_ROWS / MN_BOX_ELEMS; ++c)
             load(sb + c * MN_BOX_BYTES, &mB[part], n0 + c * MN_BOX_ELEMS, krow);
         } else {
-          load(sb, &mB[part], kb * Cf::BK, jb.b_off + n0);
+          load(sb, &mB[part], kb * Cf::BK, b_off + n0);
         }
       }
     }  // else (test hook): no bytes, no arrival -- the MMA issuer's wait on this stage runs out
@@ -492,17 +503,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       Ring ring{0, 0u};
       TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u};
+      unsigned next = (rank == 0) ? atomicAdd(&p.sched[0], 1u) : 0u;
       while (ok) {
-        const int tile = (rank == 0) ? tq.post(p.sched, p.total_tiles, units) : tq.take(1u);
+        int tile;
+        if (rank == 0) {
+          tile = tq.post(next, p.sched, p.total_tiles, units);
+          if (tile >= 0) next = atomicAdd(&p.sched[0], 1u);  // used once this tile is loaded
+        } else {
+          tile = tq.take(1u);
+        }
         if (tile < 0) break;
         const TilePos tp = locate<PAIR>(p, tile);
         const Job& jb = p.job[tp.job];
         const int m0 = tp.tm * Cf::TILE_M + static_cast<int>(rank) * BM;       // first A row here
         const int n0 = tp.tn * BN + static_cast<int>(rank) * Cf::B_ROWS * PAIR;  // first B row
         dispatch_mode<MODES>(mode_of<MODES>(jb), [&](auto m) {
-          ok = produce_tile<decltype(m)::value, PAIR, OP>(jb, maps.a[tp.job], maps.b[tp.job], m0,
-                                                          n0, base, ctl, ring, abort_flag, p.err,
-                                                          rank, p.inject_stall != 0);
+          ok = produce_tile<decltype(m)::value, PAIR, OP>(
+              jb.nkb, jb.b_off, maps.a[tp.job], maps.b[tp.job], m0, n0, base, ctl, ring,
+              abort_flag, p.err, rank, p.inject_stall != 0);
         });
       }
       if (!ok) {
@@ -1041,9 +1059,14 @@ cudaError_t run(const StripArgs* jobs, int njobs, cudaStream_t stream, int num_s
   // persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than there are tiles
   const int units = PAIR ? num_sms / 2 : num_sms;
   const int grid = (p.total_tiles < units ? p.total_tiles : units) * (PAIR ? 2 : 1);
-  // a launch never mixes the forward with the backward
-  return (p.job[0].mode == MODE_FWD_LSE) ? launch<MODES_FWD, PAIR, OP>(maps, p, grid, stream)
-                                          : launch<MODES_BWD, PAIR, OP>(maps, p, grid, stream);
+  // the kernel compiled for the modes of this launch (a launch never mixes the forward with the
+  // backward)
+  int present = 0;
+  for (int j = 0; j < p.njobs; ++j) present |= 1 << p.job[j].mode;
+  if (present == MODES_FWD) return launch<MODES_FWD, PAIR, OP>(maps, p, grid, stream);
+  if (present == MODES_G) return launch<MODES_G, PAIR, OP>(maps, p, grid, stream);
+  if ((present & ~MODES_DHDW) == 0) return launch<MODES_DHDW, PAIR, OP>(maps, p, grid, stream);
+  return launch<MODES_BWD, PAIR, OP>(maps, p, grid, stream);
 }
 
 }  // namespace
