@@ -35,10 +35,12 @@ from memory_bounded_linear_gb300.workloads import HEADLINE, WORKLOADS, make_inpu
 
 METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s vs GB300 bf16 dense peak; peak MB"
 L2_BYTES = 129 * 1024 * 1024
-# FLOPs per step of each contraction kernel, in units of N*d*V: the forward logits (2), the fused
-# backward step (recomputed logits, dH and dW: 6), and the fp32 engine's four separate kernels.
-GEMM_FLOP_FACTOR = {"tc_fwd_lse": 2, "tc_bwd": 6, "simt_fwd_lse": 2, "simt_bwd_grad": 2,
-                    "simt_dh": 2, "simt_dw": 2}
+# FLOPs per step of each contraction kernel, in units of N*d*V, summed over its launches: the
+# forward logits (2); the backward's gradient launches (recomputed logits: 2) and dH + dW launches
+# (4), or, for small backward steps, the overlapped launches that run all three (6); the fp32
+# engine's four separate kernels.
+GEMM_FLOP_FACTOR = {"tc_fwd_lse": 2, "tc_bwd_grad": 2, "tc_dh_dw": 4, "tc_bwd": 6,
+                    "simt_fwd_lse": 2, "simt_bwd_grad": 2, "simt_dh": 2, "simt_dw": 2}
 
 
 def dist_env():
@@ -399,7 +401,11 @@ def main():
                 "launches": n_launch,
                 "avg_launch_ms": t_kernel / n_launch,
                 "peak_source": peak_name,
-                "per_kernel_ms_per_step": {k: v[1] / args.steps for k, v in sorted(agg.items())}}
+                "per_kernel_ms_per_step": {k: v[1] / args.steps for k, v in sorted(agg.items())},
+                # every contraction kernel's algorithmic rate (the dominant one is above)
+                "per_kernel_tflops": {k: GEMM_FLOP_FACTOR[k] * N * d * V * x3_factor * args.steps
+                                         / (v[1] / 1e3) / 1e12
+                                      for k, v in sorted(agg.items()) if k in GEMM_FLOP_FACTOR}}
     if dt != "f32" and clk.get("sm_mhz") and clk.get("samples", 0) >= 10:
         # Context for the fraction above: the dense tensor rate per SM and clock (8192 bf16 or
         # 4096 tf32 FLOP per cycle, the per-SM rate behind the nominal 2.25 / 1.1 PFLOP/s) at the

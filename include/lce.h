@@ -239,7 +239,13 @@ lce_status_t lce_trace_begin(void* const* start_events, void* const* stop_events
                              int32_t* kernel_ids, int32_t capacity);
 int32_t lce_trace_end(void);
 
-/* Name of a traced kernel id ("tc_fwd_lse", "tc_bwd_grad", "tc_dh", "tc_dw", ...); NULL if unknown. */
+/*
+ * Name of a traced kernel id; NULL if unknown.  Tensor-core launches: "tc_fwd_lse" (forward),
+ * "tc_bwd_grad" (a strip's gradient), "tc_dh_dw" (a strip's dH and / or dW), "tc_bwd" (dH and dW
+ * of one strip with the gradient of the next, for small backward steps); CUDA-core launches of
+ * the exact fp32 path: "simt_fwd_lse", "simt_bwd_grad", "simt_dh", "simt_dw"; and "combine",
+ * "finalize", "split_tf32".
+ */
 const char* lce_kernel_name(int32_t kernel_id);
 
 #ifdef __cplusplus

@@ -381,7 +381,10 @@ lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* lab
   };
   const int64_t S = (V + strip_V - 1) / strip_V;
   auto run = [&](StripArgs* jobs, int nj) {
-    return traced(K_TC_BWD, stream, [&] { return tc_strip_jobs(jobs, nj, stream, num_sms); });
+    bool grad = false, dhdw = false;
+    for (int j = 0; j < nj; ++j) (jobs[j].mode == MODE_BWD_G ? grad : dhdw) = true;
+    const int kid = (grad && dhdw) ? K_TC_BWD : (grad ? K_TC_GRAD : K_TC_DHDW);
+    return traced(kid, stream, [&] { return tc_strip_jobs(jobs, nj, stream, num_sms); });
   };
   if (dtype == LCE_F32_TF32X3) {
     // H split once, plain (and transposed for dW).  Per strip: the W strip split, plain (and
@@ -527,9 +530,10 @@ int32_t lce_trace_end(void) {
 }
 
 const char* lce_kernel_name(int32_t id) {
-  static const char* names[K_NUM] = {"tc_fwd_lse",    "tc_bwd",  "simt_fwd_lse",
-                                     "simt_bwd_grad", "simt_dh", "simt_dw",
-                                     "combine",       "finalize", "split_tf32"};
+  static const char* names[K_NUM] = {"tc_fwd_lse",    "tc_bwd",   "simt_fwd_lse",
+                                     "simt_bwd_grad", "simt_dh",  "simt_dw",
+                                     "combine",       "finalize", "split_tf32",
+                                     "tc_bwd_grad",   "tc_dh_dw"};
   return (id >= 0 && id < K_NUM) ? names[id] : nullptr;
 }
 

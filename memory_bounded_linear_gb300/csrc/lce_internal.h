@@ -38,12 +38,13 @@ enum Mode : int {
 };
 
 // Kernel ids reported by the launch tracer.
-// K_TC_BWD is one backward step: dH and dW of one strip together with the gradient of the next.
+// K_TC_BWD is an overlapped backward step: dH and dW of one strip together with the gradient of
+// the next.  K_TC_GRAD is a strip's gradient alone; K_TC_DHDW its dH and / or dW.
 // K_SPLIT is the tf32 hi / lo split of an fp32 operand (plain or transposed).
 enum KernelId : int {
   K_TC_FWD = 0, K_TC_BWD = 1,
   K_SIMT_FWD = 2, K_SIMT_BWD_G = 3, K_SIMT_DH = 4, K_SIMT_DW = 5,
-  K_COMBINE = 6, K_FINALIZE = 7, K_SPLIT = 8, K_NUM = 9
+  K_COMBINE = 6, K_FINALIZE = 7, K_SPLIT = 8, K_TC_GRAD = 9, K_TC_DHDW = 10, K_NUM = 11
 };
 
 // Operand formats of the tensor-core engine.  OP_BF16: bf16 operands.  OP_TF32X3: fp32 operands

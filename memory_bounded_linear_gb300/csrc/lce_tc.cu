@@ -151,14 +151,21 @@ struct TcMaps {
   CUtensorMap c[MAX_JOBS][4];
 };
 
+// Suspend-time hint of every barrier wait (ns): a waiting thread sleeps in the try_wait until the
+// phase completes, up to this long, instead of returning early and polling again.  Measured 1.0-
+// 1.5% faster steps than the instruction's default, with or without the power cap.
+#ifndef LCE_WAIT_HINT_NS
+#define LCE_WAIT_HINT_NS 20000
+#endif
+
 // Bounded wait on an mbarrier phase.  Gives up after WAIT_LIMIT_NS (or at once when another role
 // already gave up), raising the CTA's abort flag and the workspace timeout bit.
 template <bool CLUSTER_ACQUIRE = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned* err) {
   auto try_once = [&]() {
-    return CLUSTER_ACQUIRE ? ptx::mbar_try_wait_cluster(bar, parity)
-                           : ptx::mbar_try_wait(bar, parity);
+    return CLUSTER_ACQUIRE ? ptx::mbar_try_wait_cluster(bar, parity, LCE_WAIT_HINT_NS)
+                           : ptx::mbar_try_wait(bar, parity, LCE_WAIT_HINT_NS);
   };
   if (try_once()) return true;
   const uint64_t t0 = ptx::globaltimer();
@@ -178,7 +185,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // Wait on a barrier regardless of the abort flag, for at most `limit_ns` (used while draining).
 __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait(bar, parity))
+  while (!ptx::mbar_try_wait(bar, parity, LCE_WAIT_HINT_NS))
     if (ptx::globaltimer() - t0 > limit_ns) return;
 }
 

@@ -35,6 +35,8 @@ def test_status_strings_and_kernel_names(lib):
     assert lib.lce_kernel_name(0) == b"tc_fwd_lse"
     assert lib.lce_kernel_name(1) == b"tc_bwd"
     assert lib.lce_kernel_name(8) == b"split_tf32"
+    assert lib.lce_kernel_name(9) == b"tc_bwd_grad"
+    assert lib.lce_kernel_name(10) == b"tc_dh_dw"
     assert lib.lce_kernel_name(-1) is None and lib.lce_kernel_name(1000) is None
 
 
