@@ -73,18 +73,14 @@ KERNEL_SOURCES = ("memory_bounded_linear_gb300/csrc/lce_tc.cu",
                   "memory_bounded_linear_gb300/csrc/ptx.cuh",
                   "memory_bounded_linear_gb300/csrc/lce_internal.h",
                   "memory_bounded_linear_gb300/csrc/lce_api.cu")  # launch structure
-KERNEL_SOURCE_SHA256 = "1ca1c5777378fa11d1a0dd6914a66ee8e94341ca7b7f942579f4b60d4d258e2a"
+KERNEL_SOURCE_SHA256 = "b9fb46b17d5d5bef176c3fe01bd9aa1e6fa69cd06ce35c28a222a0aae7e71acf"
 MEASURED_TRAFFIC = {
     # N=32768 d=6144 V=151552, strip 16384: the timed step's 21 launches -- the forward over the
-    # whole vocabulary, then per strip the gradient launch and the dW + dH launch (averaged
-    # over the 20)
-    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse", "bf16"): 30429322496,
-    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd", "bf16"): 11722072192,
-    # N=16384 d=7168 V=200000 fp32, three-product tf32, strip 16384: the timed step's 39
-    # tensor-core launches -- 13 forward strips, then per strip the gradient launch and the
-    # dH + dW launch (averaged over the 26)
-    ("n16384-d7168-v200000-fp32", 16384, "tc_fwd_lse", "tf32x3"): 14170404627,
-    ("n16384-d7168-v200000-fp32", 16384, "tc_bwd", "tf32x3"): 26676866707,
+    # whole vocabulary, then per strip the gradient launch and the dW + dH launch (each averaged
+    # over its 10 launches, the 4096-column tail strip included)
+    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse", "bf16"): 30413000000,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd_grad", "bf16"): 4475000000,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_dh_dw", "bf16"): 18763000000,
 }
 
 
