@@ -428,103 +428,76 @@ def main():
         roofline["peak_at_sampled_clock"] = p_clk
         roofline["frac_at_sampled_clock"] = achieved / p_clk
 
-    # End to end through the public API, two variants, each pipelined over K steps.
-    #  * e2e (every result back): each step copies its inputs (H, W, labels) from pinned host memory
-    #    to the device, runs forward+backward, and copies EVERY output of the call (loss, lse, dH,
-    #    dW) back to pinned host memory -- the library used as a host-to-host operator.
-    #  * e2e_loss_only (the training-loop figure): the same input copies, but only the loss comes
-    #    back; dH and dW stay on the device, where the previous layer's backward and the optimizer
-    #    use them.
-    # Three streams: inputs of step i+1 are copied in while step i computes and step i-1's results
-    # are copied out; device input and output buffers are double-buffered.
+    # End to end through the C ABI with HOST buffers (lce_forward_backward_host), two variants,
+    # each timed over K steps:
+    #  * e2e (every result back): each step's call copies H, W, labels and dloss from pinned host
+    #    memory into its device buffer, runs forward+backward, and copies EVERY output (loss, lse,
+    #    n_valid, dH, dW, error flags) back to pinned host memory -- the library used as a
+    #    host-to-host operator;
+    #  * e2e_loss_only (the training-loop figure): the same calls, but only the loss and the error
+    #    flags come back; dH and dW stay on the device, where the previous layer's backward and the
+    #    optimizer would use them.
+    # Consecutive steps alternate between two device buffers and two streams, so the copies of one
+    # step overlap the kernels of the other.
     e2e = e2e_loss = None
     if not args.no_e2e:
         Hh = H.cpu().pin_memory()
         Wh = W.cpu().pin_memory()
         yh = y.cpu().pin_memory()
-        in_bytes = sum(t.numel() * t.element_size() for t in (Hh, Wh, yh))
-        bufs = [(torch.empty_like(H), torch.empty_like(W), torch.empty_like(y)) for _ in range(2)]
-        outs = [(torch.empty((), device=dev), torch.empty(N, device=dev),
-                 torch.empty((), dtype=torch.int64, device=dev), torch.empty(N, d, device=dev),
-                 torch.empty(V, d, device=dev)) for _ in range(2)]
-        host_out = (torch.empty((), dtype=torch.float32).pin_memory(),
-                    torch.empty(N, dtype=torch.float32).pin_memory(),
-                    torch.empty(N, d, dtype=torch.float32).pin_memory(),
-                    torch.empty(V, d, dtype=torch.float32).pin_memory())
-        copy_in_stream = torch.cuda.Stream(dev)
-        copy_out_stream = torch.cuda.Stream(dev)
-        copied = [torch.cuda.Event() for _ in range(2)]
-        consumed = [torch.cuda.Event() for _ in range(2)]
-        computed = [torch.cuda.Event() for _ in range(2)]
-        drained = [torch.cuda.Event() for _ in range(2)]
+        dl = torch.ones((), dtype=torch.float32).pin_memory()
+        in_bytes = sum(t.numel() * t.element_size() for t in (Hh, Wh, yh, dl))
+        hb = api.lce_host_buffer_size(N, d, V, S, dt)
+        dbufs = [torch.empty(hb, dtype=torch.uint8, device=dev) for _ in range(2)]
+        streams = [torch.cuda.Stream(dev) for _ in range(2)]
+        houts = [{"loss": torch.empty((), dtype=torch.float32).pin_memory(),
+                  "lse": torch.empty(N, dtype=torch.float32).pin_memory(),
+                  "n_valid": torch.empty((), dtype=torch.int64).pin_memory(),
+                  "dH": torch.empty(N, d, dtype=torch.float32).pin_memory(),
+                  "dW": torch.empty(V, d, dtype=torch.float32).pin_memory(),
+                  "flags": torch.zeros(1, dtype=torch.int32).pin_memory()} for _ in range(2)]
 
-        def copy_in(i):
-            b = i % 2
-            with torch.cuda.stream(copy_in_stream):
-                if i >= 2:
-                    copy_in_stream.wait_event(consumed[b])  # step i-2 is done with this buffer
-                for dst, src in zip(bufs[b], (Hh, Wh, yh)):
-                    dst.copy_(src, non_blocking=True)
-                copied[b].record(copy_in_stream)
-
-        def compute(i, results_back):
-            b = i % 2
-            stream.wait_event(copied[b])
-            if i >= 2 and results_back:
-                stream.wait_event(drained[b])  # step i-2's results have left this buffer
-            Hd, Wd, yd = bufs[b]
-            lo, ls, n_v, dHo, dWo = outs[b]
-            api.lce_forward(Hd, Wd, yd, strip_V=S, reduction=w.reduction, workspace=ws,
-                            out=(lo, ls, n_v), stream=stream, f32_mode=fm)
-            api.lce_backward(Hd, Wd, yd, ls, n_v, one, strip_V=S, reduction=w.reduction,
-                             workspace=ws, dH=dHo, dW=dWo, stream=stream, f32_mode=fm)
-            consumed[b].record(stream)
-            if not results_back:
-                host_out[0].copy_(lo, non_blocking=True)
-                return
-            computed[b].record(stream)
-            with torch.cuda.stream(copy_out_stream):
-                copy_out_stream.wait_event(computed[b])
-                for dst, src in zip(host_out, (lo, ls, dHo, dWo)):
-                    dst.copy_(src, non_blocking=True)
-                drained[b].record(copy_out_stream)
-
-        def pipeline(k, results_back):
-            copy_in_stream.wait_stream(stream)
-            copy_out_stream.wait_stream(stream)
-            copy_in(0)
+        def run_steps(k, results_back):
             for i in range(k):
-                if i + 1 < k:
-                    copy_in(i + 1)
-                compute(i, results_back)
-            stream.wait_stream(copy_out_stream)  # the last results have reached the host
+                o = houts[i % 2]
+                outs = o if results_back else {"loss": o["loss"], "flags": o["flags"]}
+                api.lce_forward_backward_host(Hh, Wh, yh, dl, device_buffer=dbufs[i % 2],
+                                              strip_V=S, reduction=w.reduction, f32_mode=fm,
+                                              stream=streams[i % 2], **outs)
 
         def time_e2e(results_back):
-            pipeline(2, results_back)
+            run_steps(2, results_back)
             barrier()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
-            k2 = max(3, args.steps)  # the first step's copy is not overlapped: amortise it over K
+            k2 = max(3, args.steps)
             e0.record(stream)
-            pipeline(k2, results_back)
+            for st in streams:
+                st.wait_event(e0)
+            run_steps(k2, results_back)
+            for st in streams:
+                stream.wait_stream(st)
             e1.record(stream)
             barrier()
+            if any(int(o["flags"].item()) != 0 for o in houts):
+                raise RuntimeError("device error flags set during the end-to-end steps")
             return max_over_ranks(e0.elapsed_time(e1) / k2, world, dev)
 
+        out_bytes = sum(t.numel() * t.element_size() for t in houts[0].values())
         e_ms = time_e2e(True)
-        out_bytes = sum(t.numel() * t.element_size() for t in host_out)
         e2e = {"value": tokens_per_second(world, N, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
-               "ms_per_step": e_ms,
-               "results": "loss, lse, dH and dW copied back to pinned host memory every step",
-               "overlap": "inputs of step i+1 copied in and results of step i-1 copied out "
-                          "during step i"}
+               "ms_per_step": e_ms, "api": "lce_forward_backward_host",
+               "results": "loss, lse, n_valid, dH, dW and error flags copied back to pinned host "
+                          "memory every step",
+               "overlap": "two device buffers and two streams, alternating by step"}
         l_ms = time_e2e(False)
         e2e_loss = {"value": tokens_per_second(world, N, l_ms), "unit": "tokens/s",
-                    "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4, "ms_per_step": l_ms,
-                    "results": "loss only; dH and dW stay on the device (training-loop figure)",
-                    "overlap": "inputs of step i+1 copied in during step i"}
-        del bufs, outs, host_out
+                    "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4 + 4,
+                    "ms_per_step": l_ms, "api": "lce_forward_backward_host",
+                    "results": "loss and error flags only; dH and dW stay on the device "
+                               "(training-loop figure)",
+                    "overlap": "two device buffers and two streams, alternating by step"}
+        del dbufs, houts
 
     # Delayed weight gradient (lce_backward_parts): the dgrad-only and wgrad-only backward calls
     # against the fused backward on the same inputs and workspace, CUDA events on the launching

@@ -152,6 +152,36 @@ lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* lab
                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Forward and backward between HOST buffers: lce_forward followed by lce_backward, for callers
+ * whose data lives in host memory (a host-side pipeline, offloaded activations, a harness).  The
+ * call enqueues on `stream`, in this order, and returns: the copies of H, W, labels and dloss
+ * into `device_buffer`, the forward, the backward, and the copies of the requested results back
+ * to host memory.  Once the stream has passed that point (e.g. after cudaStreamSynchronize) the
+ * results are in host memory and the host inputs may be reused.
+ *   - H, W, labels, dloss: HOST inputs (layouts as in lce_forward; dloss is one fp32 value).
+ *     In page-locked (pinned) host memory the copies are asynchronous and overlap other work on
+ *     the device; pageable memory works, but then the copies may hold the calling thread.
+ *   - loss (1 float), lse (N floats), n_valid (1 int64), dH (N x d floats), dW (V x d floats),
+ *     device_error_flags (1 uint32: bit 0 a label outside [0, V) that is not ignore_index, bit 1
+ *     a kernel wait that timed out; 0 when neither happened): HOST outputs.  Any of them may be
+ *     NULL; that result is then not copied back (it is still computed).
+ *   - device_buffer: caller-owned DEVICE memory, 16-byte aligned, of at least
+ *     lce_host_buffer_size(...) bytes: it holds the workspace, the device copies of the inputs and
+ *     the results.  Two calls in flight at the same time need two buffers.
+ * Errors: as lce_forward and lce_backward (LCE_ERR_WORKSPACE_TOO_SMALL when device_bytes is below
+ * lce_host_buffer_size); problems found on the device come back through device_error_flags.
+ * The results are bitwise those of lce_forward + lce_backward on the same inputs.
+ */
+size_t lce_host_buffer_size(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dtype);
+lce_status_t lce_forward_backward_host(const void* H, const void* W, const int64_t* labels,
+                                       const float* dloss, int64_t N, int64_t d, int64_t V,
+                                       int64_t ignore_index, int64_t strip_V,
+                                       lce_reduction_t reduction, lce_dtype_t dtype, float* loss,
+                                       float* lse, int64_t* n_valid, float* dH, float* dW,
+                                       uint32_t* device_error_flags, void* device_buffer,
+                                       size_t device_bytes, void* stream);
+
+/*
  * Forward for callers that cannot allocate device memory.  The pages describe no such entry
  * point: it is an addition of this library, with no counterpart in the papers.
  *

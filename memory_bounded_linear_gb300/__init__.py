@@ -19,7 +19,8 @@ def __getattr__(name):
     # The binding is imported lazily so that host-only users (input recipes, sizes) do not need
     # torch.cuda; it never falls back to anything when the library is missing.
     if name in ("lce_workspace_size", "lce_forward", "lce_backward", "lce_check_error",
-                "lce_launch_count", "linear_cross_entropy", "LinearCrossEntropy"):
+                "lce_host_buffer_size", "lce_forward_backward_host", "lce_launch_count",
+                "linear_cross_entropy", "LinearCrossEntropy"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

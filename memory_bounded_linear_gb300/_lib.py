@@ -39,6 +39,11 @@ _SIGNATURES = {
     "lce_forward_static_scratch": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64,
                                                   _c_i64, ctypes.c_int, ctypes.c_int, _c_p, _c_p,
                                                   _c_p, _c_p, _c_p]),
+    "lce_host_buffer_size": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int]),
+    "lce_forward_backward_host": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
+                                                 _c_i64, _c_i64, ctypes.c_int, ctypes.c_int, _c_p,
+                                                 _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                                 ctypes.c_size_t, _c_p]),
     "lce_check_error": (ctypes.c_int, [_c_p, _c_p]),
     "lce_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "lce_last_cuda_error": (ctypes.c_char_p, []),

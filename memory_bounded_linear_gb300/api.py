@@ -141,6 +141,46 @@ def lce_backward(H, W, labels, lse, n_valid, dloss, *, ignore_index: int = -100,
     return dH, dW, workspace
 
 
+def lce_host_buffer_size(N: int, d: int, V: int, strip_V: int, dtype: str = "bf16") -> int:
+    """Device-buffer bytes lce_forward_backward_host needs for these sizes (0 on a bad shape)."""
+    return int(_lib.load().lce_host_buffer_size(N, d, V, strip_V, _lib.DTYPES[dtype]))
+
+
+def lce_forward_backward_host(H, W, labels, dloss, *, device_buffer: torch.Tensor,
+                              ignore_index: int = -100, strip_V: int = 8192,
+                              reduction: str = "mean", f32_mode: str = "exact", loss=None,
+                              lse=None, n_valid=None, dH=None, dW=None, flags=None,
+                              stream: Optional[torch.cuda.Stream] = None):
+    """Run the host-buffer entry point: H [N, d], W [V, d], labels [N] and dloss [] are CPU
+    tensors (pinned for asynchronous copies); loss, lse, n_valid, dH, dW and flags are CPU
+    tensors the results are copied into, or None to skip that copy.  device_buffer is a CUDA
+    uint8 tensor of at least lce_host_buffer_size bytes.  Only enqueues work on the stream."""
+    for t in (H, W, labels, dloss):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("H, W, labels and dloss must be contiguous CPU tensors")
+    if H.dim() != 2 or W.dim() != 2 or labels.dim() != 1 or H.shape[1] != W.shape[1] or \
+            labels.shape[0] != H.shape[0] or H.dtype != W.dtype or labels.dtype != torch.int64:
+        raise ValueError("expected H [N, d], W [V, d] of one dtype and int64 labels [N]")
+    if dloss.dtype != torch.float32 or dloss.numel() != 1:
+        raise ValueError("dloss must be one float32 value")
+    for t in (loss, lse, n_valid, dH, dW, flags):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("outputs must be contiguous CPU tensors")
+    if not device_buffer.is_cuda:
+        raise ValueError("device_buffer must be a CUDA tensor")
+    N, d = H.shape
+    V = W.shape[0]
+    dt = _dtype_name(H, f32_mode)
+    dev = device_buffer.device
+    with torch.cuda.device(dev):
+        st = _lib.load().lce_forward_backward_host(
+            _ptr(H), _ptr(W), _ptr(labels), _ptr(dloss), N, d, V, ignore_index, strip_V,
+            _lib.REDUCTIONS[reduction], _lib.DTYPES[dt], _ptr(loss), _ptr(lse), _ptr(n_valid),
+            _ptr(dH), _ptr(dW), _ptr(flags), _ptr(device_buffer), device_buffer.numel(),
+            _stream_handle(dev, stream))
+    _lib.check(st, "lce_forward_backward_host")
+
+
 def lce_check_error(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
     """Synchronise and raise if the device flagged a bad label or a timed-out wait."""
     with torch.cuda.device(workspace.device):

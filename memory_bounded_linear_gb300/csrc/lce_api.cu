@@ -104,6 +104,38 @@ bool make_layout(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t d
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device buffer of lce_forward_backward_host: the workspace, then the device copies of the inputs
+// (H, W, labels, dloss) and the results (loss, n_valid, lse, dH, dW), each 256-byte aligned.
+struct HostLayout {
+  size_t ws, off_H, off_W, off_y, off_dloss, off_loss, off_nv, off_lse, off_dH, off_dW, total;
+};
+
+bool make_host_layout(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dt,
+                      HostLayout* h) {
+  Layout L;
+  if (!make_layout(N, d, V, strip_V, dt, &L)) return false;
+  const size_t n = static_cast<size_t>(N), dd = static_cast<size_t>(d), v = static_cast<size_t>(V);
+  const size_t elt = (dt == LCE_BF16) ? 2 : 4;
+  h->ws = L.total;
+  size_t off = align256(L.total);
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  h->off_H = take(n * dd * elt);
+  h->off_W = take(v * dd * elt);
+  h->off_y = take(n * sizeof(int64_t));
+  h->off_dloss = take(sizeof(float));
+  h->off_loss = take(sizeof(float));
+  h->off_nv = take(sizeof(int64_t));
+  h->off_lse = take(n * sizeof(float));
+  h->off_dH = take(n * dd * sizeof(float));
+  h->off_dW = take(v * dd * sizeof(float));
+  h->total = off;
+  return true;
+}
+
 // --------------------------------------------------------------------------- device checks
 thread_local char g_last_error[384] = "none";
 thread_local bool g_detail_set = false;
@@ -327,12 +359,20 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels, in
   return LCE_OK;
 }
 
-lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* labels,
-                                const float* lse, const int64_t* n_valid, const float* dloss,
-                                int64_t N, int64_t d, int64_t V, int64_t ignore_index,
-                                int64_t strip_V, lce_reduction_t reduction, lce_dtype_t dtype,
-                                int32_t parts, float* dH, float* dW, void* workspace,
-                                size_t ws_bytes, void* stream_) {
+}  // extern "C"
+
+namespace lce {
+namespace {
+
+// The backward.  keep_flags: leave the error flags (header word 0) as the forward left them, so
+// that one flag word reports both passes (lce_forward_backward_host); the rest of the header (the
+// tile scheduler's counters) is cleared either way.
+lce_status_t backward_impl(const void* H, const void* W, const int64_t* labels, const float* lse,
+                           const int64_t* n_valid, const float* dloss, int64_t N, int64_t d,
+                           int64_t V, int64_t ignore_index, int64_t strip_V,
+                           lce_reduction_t reduction, lce_dtype_t dtype, int32_t parts, float* dH,
+                           float* dW, void* workspace, size_t ws_bytes, void* stream_,
+                           bool keep_flags) {
   Layout L;
   lce_status_t st = common_checks(H, W, labels, N, d, V, strip_V, reduction, dtype, workspace,
                                   ws_bytes, &L);
@@ -351,7 +391,9 @@ lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* lab
   unsigned* err = reinterpret_cast<unsigned*>(ws);
   void* G = ws + L.off_g;
   // error flags and scheduler counters start from zero (the workspace may be fresh memory)
-  if (note(cudaMemsetAsync(ws, 0, WS_HEADER_BYTES, stream)) != cudaSuccess) return LCE_ERR_CUDA;
+  const size_t keep = keep_flags ? sizeof(unsigned) : 0;
+  if (note(cudaMemsetAsync(ws + keep, 0, WS_HEADER_BYTES - keep, stream)) != cudaSuccess)
+    return LCE_ERR_CUDA;
   if (N == 0) {
     // no token: every logit-gradient row is absent, so dW = 0 (dH has no rows)
     if (want_dw &&
@@ -458,6 +500,21 @@ lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* lab
   return LCE_OK;
 }
 
+}  // namespace
+}  // namespace lce
+
+extern "C" {
+
+lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* labels,
+                                const float* lse, const int64_t* n_valid, const float* dloss,
+                                int64_t N, int64_t d, int64_t V, int64_t ignore_index,
+                                int64_t strip_V, lce_reduction_t reduction, lce_dtype_t dtype,
+                                int32_t parts, float* dH, float* dW, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  return backward_impl(H, W, labels, lse, n_valid, dloss, N, d, V, ignore_index, strip_V,
+                       reduction, dtype, parts, dH, dW, workspace, ws_bytes, stream, false);
+}
+
 lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, const float* lse,
                           const int64_t* n_valid, const float* dloss, int64_t N, int64_t d, int64_t V,
                           int64_t ignore_index, int64_t strip_V, lce_reduction_t reduction,
@@ -466,6 +523,71 @@ lce_status_t lce_backward(const void* H, const void* W, const int64_t* labels, c
   return lce_backward_parts(H, W, labels, lse, n_valid, dloss, N, d, V, ignore_index, strip_V,
                             reduction, dtype, LCE_GRAD_DH | LCE_GRAD_DW, dH, dW, workspace,
                             ws_bytes, stream);
+}
+
+size_t lce_host_buffer_size(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dtype) {
+  HostLayout h;
+  if (!make_host_layout(N, d, V, strip_V, dtype, &h)) return 0;
+  return h.total;
+}
+
+lce_status_t lce_forward_backward_host(const void* H, const void* W, const int64_t* labels,
+                                       const float* dloss, int64_t N, int64_t d, int64_t V,
+                                       int64_t ignore_index, int64_t strip_V,
+                                       lce_reduction_t reduction, lce_dtype_t dtype, float* loss,
+                                       float* lse, int64_t* n_valid, float* dH, float* dW,
+                                       uint32_t* device_error_flags, void* device_buffer,
+                                       size_t device_bytes, void* stream_) {
+  // host-side validation first: nothing reaches the CUDA runtime on a bad argument
+  if (reduction != LCE_REDUCTION_MEAN && reduction != LCE_REDUCTION_SUM) return LCE_ERR_INVALID_ARG;
+  if (dtype != LCE_BF16 && dtype != LCE_F32 && dtype != LCE_F32_TF32X3) return LCE_ERR_INVALID_ARG;
+  if (!W || !dloss || !device_buffer || (N > 0 && (!H || !labels))) return LCE_ERR_INVALID_ARG;
+  if (!aligned16(device_buffer)) return LCE_ERR_INVALID_ARG;
+  HostLayout h;
+  if (!make_host_layout(N, d, V, strip_V, dtype, &h)) return LCE_ERR_UNSUPPORTED_SHAPE;
+  if (device_bytes < h.total) return LCE_ERR_WORKSPACE_TOO_SMALL;
+  int num_sms = 0;
+  lce_status_t st = check_device(&num_sms);
+  if (st != LCE_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+  char* buf = static_cast<char*>(device_buffer);
+  const size_t n = static_cast<size_t>(N), dd = static_cast<size_t>(d), v = static_cast<size_t>(V);
+  const size_t elt = (dtype == LCE_BF16) ? 2 : 4;
+  void* dH_in = buf + h.off_H;
+  void* dW_in = buf + h.off_W;
+  int64_t* d_y = reinterpret_cast<int64_t*>(buf + h.off_y);
+  float* d_dloss = reinterpret_cast<float*>(buf + h.off_dloss);
+  float* d_loss = reinterpret_cast<float*>(buf + h.off_loss);
+  int64_t* d_nv = reinterpret_cast<int64_t*>(buf + h.off_nv);
+  float* d_lse = reinterpret_cast<float*>(buf + h.off_lse);
+  float* d_dH = reinterpret_cast<float*>(buf + h.off_dH);
+  float* d_dW = reinterpret_cast<float*>(buf + h.off_dW);
+  auto copy = [&](void* dst, const void* src, size_t bytes, cudaMemcpyKind kind) {
+    return bytes == 0 || note(cudaMemcpyAsync(dst, src, bytes, kind, stream)) == cudaSuccess;
+  };
+  if (!copy(dH_in, H, n * dd * elt, cudaMemcpyHostToDevice) ||
+      !copy(dW_in, W, v * dd * elt, cudaMemcpyHostToDevice) ||
+      !copy(d_y, labels, n * sizeof(int64_t), cudaMemcpyHostToDevice) ||
+      !copy(d_dloss, dloss, sizeof(float), cudaMemcpyHostToDevice))
+    return LCE_ERR_CUDA;
+  st = lce_forward(dH_in, dW_in, d_y, N, d, V, ignore_index, strip_V, reduction, dtype, d_loss,
+                   d_lse, d_nv, buf, h.ws, stream_);
+  if (st != LCE_OK) return st;
+  // the backward keeps the forward's error bits and adds its own
+  st = backward_impl(dH_in, dW_in, d_y, d_lse, d_nv, d_dloss, N, d, V, ignore_index, strip_V,
+                     reduction, dtype, LCE_GRAD_DH | LCE_GRAD_DW, d_dH, d_dW, buf, h.ws, stream_,
+                     true);
+  if (st != LCE_OK) return st;
+  if ((loss && !copy(loss, d_loss, sizeof(float), cudaMemcpyDeviceToHost)) ||
+      (n_valid && !copy(n_valid, d_nv, sizeof(int64_t), cudaMemcpyDeviceToHost)) ||
+      (lse && !copy(lse, d_lse, n * sizeof(float), cudaMemcpyDeviceToHost)) ||
+      (dH && !copy(dH, d_dH, n * dd * sizeof(float), cudaMemcpyDeviceToHost)) ||
+      (dW && !copy(dW, d_dW, v * dd * sizeof(float), cudaMemcpyDeviceToHost)) ||
+      (device_error_flags &&
+       !copy(device_error_flags, buf, sizeof(uint32_t), cudaMemcpyDeviceToHost)))
+    return LCE_ERR_CUDA;
+  return LCE_OK;
 }
 
 lce_status_t lce_check_error(const void* workspace, void* stream_) {

@@ -179,3 +179,51 @@ def test_check_error_and_trace_argument_validation(lib):
     assert lib.lce_trace_begin(None, None, None, 0) == 0
     assert lib.lce_trace_end() == 0
     assert lib.lce_launch_count() >= 0
+
+
+def test_host_buffer_size_layout(lib):
+    """The host-buffer entry point's device buffer: the workspace, then the device copies of the
+    inputs and the results, each 256-byte aligned."""
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for (N, d, V, s, dt, elt) in [(32768, 6144, 151552, 16384, 0, 2), (100, 64, 300, 4096, 0, 2),
+                                  (256, 256, 4096, 512, 1, 4), (33, 8, 1000, 128, 2, 4),
+                                  (0, 64, 300, 128, 0, 2)]:
+        ws = _ws(lib, N, d, V, s, dt)
+        want = (r(ws) + r(N * d * elt) + r(V * d * elt) + r(N * 8) + 3 * 256 + r(N * 4)
+                + r(N * d * 4) + r(V * d * 4))
+        assert lib.lce_host_buffer_size(N, d, V, s, dt) == want, (N, d, V, s, dt)
+    assert lib.lce_host_buffer_size(100, 60, 300, 128, 0) == 0   # d % 8 != 0 for bf16
+    assert lib.lce_host_buffer_size(100, 64, 300, 100, 0) == 0   # strip not a multiple of 128
+
+
+def test_host_entry_point_rejects_bad_arguments_on_the_host(lib):
+    """Every argument error of lce_forward_backward_host comes back before any CUDA call."""
+    f = lib.lce_forward_backward_host
+    buf = ctypes.create_string_buffer(1 << 20)
+    addr = (ctypes.addressof(buf) + 255) // 256 * 256  # stands in for device memory: never touched
+    one = (ctypes.c_float * 1)(1.0)
+    H = (ctypes.c_uint16 * 64)()
+    W = (ctypes.c_uint16 * (64 * 300))()
+    y = (ctypes.c_int64 * 1)()
+    ok_args = [H, W, y, one, 1, 64, 300, -100, 128, 0, 0, None, None, None, None, None, None,
+               addr, 1 << 19, None]
+
+    def call(**kw):
+        a = list(ok_args)
+        names = ["H", "W", "y", "dloss", "N", "d", "V", "ign", "strip", "red", "dt", "loss", "lse",
+                 "nv", "dH", "dW", "flags", "buf", "bytes", "stream"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return _lib.STATUS_NAMES[f(*a)]
+
+    assert call(red=7) == "LCE_ERR_INVALID_ARG"
+    assert call(dt=9) == "LCE_ERR_INVALID_ARG"
+    assert call(W=None) == "LCE_ERR_INVALID_ARG"
+    assert call(dloss=None) == "LCE_ERR_INVALID_ARG"
+    assert call(buf=None) == "LCE_ERR_INVALID_ARG"
+    assert call(buf=addr + 8) == "LCE_ERR_INVALID_ARG"         # not 16-byte aligned
+    assert call(H=None) == "LCE_ERR_INVALID_ARG"               # N > 0 needs H and labels
+    assert call(d=60) == "LCE_ERR_UNSUPPORTED_SHAPE"
+    assert call(strip=100) == "LCE_ERR_UNSUPPORTED_SHAPE"
+    need = lib.lce_host_buffer_size(1, 64, 300, 128, 0)
+    assert call(bytes=need - 1) == "LCE_ERR_WORKSPACE_TOO_SMALL"

@@ -1,0 +1,126 @@
+"""The host-buffer entry point (lce_forward_backward_host): inputs and results in host memory, one
+caller-owned device buffer.  Through the C ABI, its results must be bitwise those of
+lce_forward + lce_backward on device copies of the same inputs (the same kernels run on the same
+values), for every input format and both backward schedules, and match the float64 oracle;
+device-side errors come back through the flags output; results not asked for are not copied;
+two calls in flight on two streams with two buffers do not disturb each other."""
+
+import numpy as np
+import pytest
+import torch
+
+from memory_bounded_linear_gb300 import api
+from memory_bounded_linear_gb300.workloads import WORKLOADS, make_inputs
+
+from ._parity import assert_parity, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+W2 = WORKLOADS["n4096-d2048-v151936"]
+W3 = WORKLOADS["n16384-d4096-v131072-ignore10"]
+WT = WORKLOADS["tiny-fp32"]
+
+CASES = [
+    (W3.with_sizes(N=517, d=256, V=2048, strip_V=512), "exact"),     # bf16, overlapped backward
+    (W2.with_sizes(N=4352, d=8192, V=700, strip_V=512), "exact"),    # bf16, separate launches
+    (WT.with_sizes(N=300, d=136, V=1000, strip_V=384), "exact"),     # fp32 on the CUDA cores
+    (WT.with_sizes(N=300, d=136, V=1000, strip_V=384, reduction="sum"), "tf32x3"),
+]
+IDS = ["bf16-overlap", "bf16-large-step", "f32", "tf32x3-sum"]
+
+
+def _host_outputs(N, d, V):
+    return {"loss": torch.full((), float("nan")).pin_memory(),
+            "lse": torch.full((N,), float("nan")).pin_memory(),
+            "n_valid": torch.full((), -1, dtype=torch.int64).pin_memory(),
+            "dH": torch.full((N, d), float("nan")).pin_memory(),
+            "dW": torch.full((V, d), float("nan")).pin_memory(),
+            "flags": torch.full((1,), 0x7F7F7F7F, dtype=torch.int32).pin_memory()}
+
+
+def _host_run(H, W, y, w, mode, skip=(), stream=None, buffer=None, outs=None):
+    dt = "tf32x3" if (w.dtype == "f32" and mode == "tf32x3") else w.dtype
+    N, d, V = w.N, w.d, w.V
+    if buffer is None:
+        buffer = torch.empty(api.lce_host_buffer_size(N, d, V, w.strip_V, dt), dtype=torch.uint8,
+                             device="cuda")
+    outs = outs or _host_outputs(N, d, V)
+    kw = {k: (None if k in skip else v) for k, v in outs.items()}
+    # the pinned inputs and the device buffer must outlive the copies the call enqueued: they are
+    # returned with the outputs and kept until the caller has synchronised
+    pinned = (H.pin_memory(), W.pin_memory(), y.pin_memory(),
+              torch.ones((), dtype=torch.float32).pin_memory())
+    api.lce_forward_backward_host(*pinned, device_buffer=buffer, strip_V=w.strip_V,
+                                  reduction=w.reduction, f32_mode=mode, stream=stream, **kw)
+    outs["_keep"] = (pinned, buffer)
+    return outs
+
+
+def _device_run(H, W, y, w, mode):
+    Hd, Wd, yd = H.cuda(), W.cuda(), y.cuda()
+    loss, lse, nv, ws = api.lce_forward(Hd, Wd, yd, strip_V=w.strip_V, reduction=w.reduction,
+                                        f32_mode=mode)
+    dH, dW, _ = api.lce_backward(Hd, Wd, yd, lse, nv, torch.ones((), device="cuda"),
+                                 strip_V=w.strip_V, reduction=w.reduction, workspace=ws,
+                                 f32_mode=mode)
+    torch.cuda.synchronize()
+    return {"loss": loss.cpu(), "lse": lse.cpu(), "n_valid": nv.cpu(), "dH": dH.cpu(),
+            "dW": dW.cpu()}
+
+
+@pytest.mark.parametrize("w,mode", CASES, ids=IDS)
+def test_host_entry_point_matches_device_entry_points_bitwise(cuda_lib, w, mode):
+    H, W, y = make_inputs(w, "cpu", seed=11)
+    out = _host_run(H, W, y, w, mode)
+    torch.cuda.synchronize()
+    ref = _device_run(H, W, y, w, mode)
+    assert int(out["flags"].item()) == 0
+    for k in ("loss", "lse", "n_valid", "dH", "dW"):
+        assert torch.equal(out[k], ref[k]), k
+    g = {"loss": out["loss"].item(), "lse": out["lse"].double().numpy(),
+         "n_valid": int(out["n_valid"].item()), "dH": out["dH"].double().numpy(),
+         "dW": out["dW"].double().numpy()}
+    r = run_oracle(H, W, y, w.reduction)
+    assert_parity(g, r, "tf32x3" if mode == "tf32x3" else w.dtype)
+
+
+@pytest.mark.parametrize("w,mode", [CASES[0], CASES[3]], ids=["bf16", "tf32x3"])
+def test_host_entry_point_reports_bad_label(cuda_lib, w, mode):
+    H, W, y = make_inputs(w, "cpu", seed=12)
+    y[3] = w.V
+    y[w.N - 1] = -5
+    out = _host_run(H, W, y, w, mode)
+    torch.cuda.synchronize()
+    assert int(out["flags"].item()) == 1
+    r = run_oracle(H, W, y, w.reduction)
+    assert int(out["n_valid"].item()) == r["n_valid"]
+    assert torch.count_nonzero(out["dH"][[3, w.N - 1]]).item() == 0
+
+
+def test_host_entry_point_skips_results_not_asked_for(cuda_lib):
+    w, mode = CASES[0]
+    H, W, y = make_inputs(w, "cpu", seed=13)
+    out = _host_run(H, W, y, w, mode, skip=("lse", "dW", "flags"))
+    torch.cuda.synchronize()
+    ref = _device_run(H, W, y, w, mode)
+    assert torch.isnan(out["lse"]).all() and torch.isnan(out["dW"]).all()
+    assert int(out["flags"].item()) == 0x7F7F7F7F
+    assert torch.equal(out["loss"], ref["loss"]) and torch.equal(out["dH"], ref["dH"])
+
+
+def test_two_host_calls_in_flight_on_two_streams(cuda_lib):
+    """Two calls, each with its own device buffer, enqueued on two streams back to back: each
+    returns its own inputs' results."""
+    w, mode = CASES[1]
+    inputs = [make_inputs(w, "cpu", seed=s) for s in (21, 22)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for (H, W, y), st in zip(inputs, streams):
+        outs.append(_host_run(H, W, y, w, mode, stream=st))
+    torch.cuda.synchronize()
+    for (H, W, y), out in zip(inputs, outs):
+        ref = _device_run(H, W, y, w, mode)
+        assert int(out["flags"].item()) == 0
+        for k in ("loss", "lse", "dH", "dW"):
+            assert torch.equal(out[k], ref[k]), k
+    assert not np.array_equal(outs[0]["dW"].numpy(), outs[1]["dW"].numpy())
