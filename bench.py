@@ -456,13 +456,19 @@ def main():
                   "dW": torch.empty(V, d, dtype=torch.float32).pin_memory(),
                   "flags": torch.zeros(1, dtype=torch.int32).pin_memory()} for _ in range(2)]
 
+        done = [torch.cuda.Event() for _ in range(2)]
+
         def run_steps(k, results_back):
             for i in range(k):
                 o = houts[i % 2]
                 outs = o if results_back else {"loss": o["loss"], "flags": o["flags"]}
+                # this step's kernels start after the previous step's have finished: the copies
+                # overlap the other step's kernels, the kernels run one step at a time
                 api.lce_forward_backward_host(Hh, Wh, yh, dl, device_buffer=dbufs[i % 2],
                                               strip_V=S, reduction=w.reduction, f32_mode=fm,
-                                              stream=streams[i % 2], **outs)
+                                              stream=streams[i % 2],
+                                              compute_after=done[(i + 1) % 2] if i else None,
+                                              compute_done=done[i % 2], **outs)
 
         def time_e2e(results_back):
             run_steps(2, results_back)
@@ -489,14 +495,16 @@ def main():
                "ms_per_step": e_ms, "api": "lce_forward_backward_host",
                "results": "loss, lse, n_valid, dH, dW and error flags copied back to pinned host "
                           "memory every step",
-               "overlap": "two device buffers and two streams, alternating by step"}
+               "overlap": "two device buffers and two streams alternating by step; each step's "
+                          "kernels wait for the previous step's (compute_after / compute_done)"}
         l_ms = time_e2e(False)
         e2e_loss = {"value": tokens_per_second(world, N, l_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4 + 4,
                     "ms_per_step": l_ms, "api": "lce_forward_backward_host",
                     "results": "loss and error flags only; dH and dW stay on the device "
                                "(training-loop figure)",
-                    "overlap": "two device buffers and two streams, alternating by step"}
+                    "overlap": "two device buffers and two streams alternating by step; each "
+                               "step's kernels wait for the previous step's"}
         del dbufs, houts
 
     # Delayed weight gradient (lce_backward_parts): the dgrad-only and wgrad-only backward calls

@@ -168,6 +168,13 @@ lce_status_t lce_backward_parts(const void* H, const void* W, const int64_t* lab
  *   - device_buffer: caller-owned DEVICE memory, 16-byte aligned, of at least
  *     lce_host_buffer_size(...) bytes: it holds the workspace, the device copies of the inputs and
  *     the results.  Two calls in flight at the same time need two buffers.
+ *   - compute_after, compute_done: optional cudaEvent_t handles (NULL for none), owned by the
+ *     caller.  The kernels of this call start only once compute_after has completed (a wait
+ *     enqueued after the input copies), and compute_done is recorded once they have finished
+ *     (before the result copies).  With them a caller runs consecutive calls on two streams and
+ *     two buffers so that one call's copies overlap the other's kernels while the kernels of
+ *     the calls still run one after another (kernels of two calls running at the same time
+ *     share the SMs and slow each other down).
  * Errors: as lce_forward and lce_backward (LCE_ERR_WORKSPACE_TOO_SMALL when device_bytes is below
  * lce_host_buffer_size); problems found on the device come back through device_error_flags.
  * The results are bitwise those of lce_forward + lce_backward on the same inputs.
@@ -179,7 +186,8 @@ lce_status_t lce_forward_backward_host(const void* H, const void* W, const int64
                                        lce_reduction_t reduction, lce_dtype_t dtype, float* loss,
                                        float* lse, int64_t* n_valid, float* dH, float* dW,
                                        uint32_t* device_error_flags, void* device_buffer,
-                                       size_t device_bytes, void* stream);
+                                       size_t device_bytes, void* stream,
+                                       const void* compute_after, void* compute_done);
 
 /*
  * Forward for callers that cannot allocate device memory.  The pages describe no such entry

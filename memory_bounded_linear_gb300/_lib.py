@@ -43,7 +43,7 @@ _SIGNATURES = {
     "lce_forward_backward_host": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
                                                  _c_i64, _c_i64, ctypes.c_int, ctypes.c_int, _c_p,
                                                  _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
-                                                 ctypes.c_size_t, _c_p]),
+                                                 ctypes.c_size_t, _c_p, _c_p, _c_p]),
     "lce_check_error": (ctypes.c_int, [_c_p, _c_p]),
     "lce_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "lce_last_cuda_error": (ctypes.c_char_p, []),

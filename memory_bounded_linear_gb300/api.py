@@ -39,6 +39,15 @@ def _stream_handle(device: torch.device, stream: Optional[torch.cuda.Stream]) ->
     return s.cuda_stream
 
 
+def _event_handle(e: Optional[torch.cuda.Event]) -> Optional[int]:
+    """The cudaEvent_t of a torch event (torch creates the CUDA event at its first record)."""
+    if e is None:
+        return None
+    if not e.cuda_event:
+        e.record()
+    return e.cuda_event
+
+
 def _check_inputs(H, W, labels):
     if not (H.is_cuda and W.is_cuda and labels.is_cuda):
         raise ValueError("H, W and labels must be CUDA tensors")
@@ -150,11 +159,15 @@ def lce_forward_backward_host(H, W, labels, dloss, *, device_buffer: torch.Tenso
                               ignore_index: int = -100, strip_V: int = 8192,
                               reduction: str = "mean", f32_mode: str = "exact", loss=None,
                               lse=None, n_valid=None, dH=None, dW=None, flags=None,
-                              stream: Optional[torch.cuda.Stream] = None):
+                              stream: Optional[torch.cuda.Stream] = None,
+                              compute_after: Optional[torch.cuda.Event] = None,
+                              compute_done: Optional[torch.cuda.Event] = None):
     """Run the host-buffer entry point: H [N, d], W [V, d], labels [N] and dloss [] are CPU
     tensors (pinned for asynchronous copies); loss, lse, n_valid, dH, dW and flags are CPU
     tensors the results are copied into, or None to skip that copy.  device_buffer is a CUDA
-    uint8 tensor of at least lce_host_buffer_size bytes.  Only enqueues work on the stream."""
+    uint8 tensor of at least lce_host_buffer_size bytes.  compute_after / compute_done: events
+    the call's kernels wait for / record when they are done (see include/lce.h).  Only enqueues
+    work on the stream."""
     for t in (H, W, labels, dloss):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError("H, W, labels and dloss must be contiguous CPU tensors")
@@ -177,7 +190,8 @@ def lce_forward_backward_host(H, W, labels, dloss, *, device_buffer: torch.Tenso
             _ptr(H), _ptr(W), _ptr(labels), _ptr(dloss), N, d, V, ignore_index, strip_V,
             _lib.REDUCTIONS[reduction], _lib.DTYPES[dt], _ptr(loss), _ptr(lse), _ptr(n_valid),
             _ptr(dH), _ptr(dW), _ptr(flags), _ptr(device_buffer), device_buffer.numel(),
-            _stream_handle(dev, stream))
+            _stream_handle(dev, stream), _event_handle(compute_after),
+            _event_handle(compute_done))
     _lib.check(st, "lce_forward_backward_host")
 
 

@@ -537,7 +537,8 @@ lce_status_t lce_forward_backward_host(const void* H, const void* W, const int64
                                        lce_reduction_t reduction, lce_dtype_t dtype, float* loss,
                                        float* lse, int64_t* n_valid, float* dH, float* dW,
                                        uint32_t* device_error_flags, void* device_buffer,
-                                       size_t device_bytes, void* stream_) {
+                                       size_t device_bytes, void* stream_,
+                                       const void* compute_after, void* compute_done) {
   // host-side validation first: nothing reaches the CUDA runtime on a bad argument
   if (reduction != LCE_REDUCTION_MEAN && reduction != LCE_REDUCTION_SUM) return LCE_ERR_INVALID_ARG;
   if (dtype != LCE_BF16 && dtype != LCE_F32 && dtype != LCE_F32_TF32X3) return LCE_ERR_INVALID_ARG;
@@ -571,6 +572,10 @@ lce_status_t lce_forward_backward_host(const void* H, const void* W, const int64
       !copy(d_y, labels, n * sizeof(int64_t), cudaMemcpyHostToDevice) ||
       !copy(d_dloss, dloss, sizeof(float), cudaMemcpyHostToDevice))
     return LCE_ERR_CUDA;
+  if (compute_after &&
+      note(cudaStreamWaitEvent(stream, static_cast<cudaEvent_t>(const_cast<void*>(compute_after)),
+                               0)) != cudaSuccess)
+    return LCE_ERR_CUDA;
   st = lce_forward(dH_in, dW_in, d_y, N, d, V, ignore_index, strip_V, reduction, dtype, d_loss,
                    d_lse, d_nv, buf, h.ws, stream_);
   if (st != LCE_OK) return st;
@@ -579,6 +584,9 @@ lce_status_t lce_forward_backward_host(const void* H, const void* W, const int64
                      reduction, dtype, LCE_GRAD_DH | LCE_GRAD_DW, d_dH, d_dW, buf, h.ws, stream_,
                      true);
   if (st != LCE_OK) return st;
+  if (compute_done &&
+      note(cudaEventRecord(static_cast<cudaEvent_t>(compute_done), stream)) != cudaSuccess)
+    return LCE_ERR_CUDA;
   if ((loss && !copy(loss, d_loss, sizeof(float), cudaMemcpyDeviceToHost)) ||
       (n_valid && !copy(n_valid, d_nv, sizeof(int64_t), cudaMemcpyDeviceToHost)) ||
       (lse && !copy(lse, d_lse, n * sizeof(float), cudaMemcpyDeviceToHost)) ||

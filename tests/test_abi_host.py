@@ -206,12 +206,12 @@ def test_host_entry_point_rejects_bad_arguments_on_the_host(lib):
     W = (ctypes.c_uint16 * (64 * 300))()
     y = (ctypes.c_int64 * 1)()
     ok_args = [H, W, y, one, 1, 64, 300, -100, 128, 0, 0, None, None, None, None, None, None,
-               addr, 1 << 19, None]
+               addr, 1 << 19, None, None, None]
 
     def call(**kw):
         a = list(ok_args)
         names = ["H", "W", "y", "dloss", "N", "d", "V", "ign", "strip", "red", "dt", "loss", "lse",
-                 "nv", "dH", "dW", "flags", "buf", "bytes", "stream"]
+                 "nv", "dH", "dW", "flags", "buf", "bytes", "stream", "after", "done"]
         for k, v in kw.items():
             a[names.index(k)] = v
         return _lib.STATUS_NAMES[f(*a)]

@@ -38,7 +38,8 @@ def _host_outputs(N, d, V):
             "flags": torch.full((1,), 0x7F7F7F7F, dtype=torch.int32).pin_memory()}
 
 
-def _host_run(H, W, y, w, mode, skip=(), stream=None, buffer=None, outs=None):
+def _host_run(H, W, y, w, mode, skip=(), stream=None, buffer=None, outs=None, after=None,
+              done=None):
     dt = "tf32x3" if (w.dtype == "f32" and mode == "tf32x3") else w.dtype
     N, d, V = w.N, w.d, w.V
     if buffer is None:
@@ -51,7 +52,8 @@ def _host_run(H, W, y, w, mode, skip=(), stream=None, buffer=None, outs=None):
     pinned = (H.pin_memory(), W.pin_memory(), y.pin_memory(),
               torch.ones((), dtype=torch.float32).pin_memory())
     api.lce_forward_backward_host(*pinned, device_buffer=buffer, strip_V=w.strip_V,
-                                  reduction=w.reduction, f32_mode=mode, stream=stream, **kw)
+                                  reduction=w.reduction, f32_mode=mode, stream=stream,
+                                  compute_after=after, compute_done=done, **kw)
     outs["_keep"] = (pinned, buffer)
     return outs
 
@@ -124,3 +126,30 @@ def test_two_host_calls_in_flight_on_two_streams(cuda_lib):
         for k in ("loss", "lse", "dH", "dW"):
             assert torch.equal(out[k], ref[k]), k
     assert not np.array_equal(outs[0]["dW"].numpy(), outs[1]["dW"].numpy())
+
+
+def test_host_calls_chained_by_compute_events(cuda_lib):
+    """Four calls alternating between two streams and two buffers, each call's kernels waiting
+    for the previous call's (compute_after / compute_done), as a pipelined caller runs them: every
+    call returns its own inputs' results, and the kernels of consecutive calls do not overlap in
+    time."""
+    w, mode = CASES[0]
+    inputs = [make_inputs(w, "cpu", seed=s) for s in (31, 32, 33, 34)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    done = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    dt = "bf16"
+    buffers = [torch.empty(api.lce_host_buffer_size(w.N, w.d, w.V, w.strip_V, dt),
+                           dtype=torch.uint8, device="cuda") for _ in range(2)]
+    outs = []
+    for i, (H, W, y) in enumerate(inputs):
+        outs.append(_host_run(H, W, y, w, mode, stream=streams[i % 2], buffer=buffers[i % 2],
+                              after=done[i - 1] if i else None, done=done[i]))
+    torch.cuda.synchronize()
+    for (H, W, y), out in zip(inputs, outs):
+        ref = _device_run(H, W, y, w, mode)
+        assert int(out["flags"].item()) == 0
+        for k in ("loss", "lse", "dH", "dW"):
+            assert torch.equal(out[k], ref[k]), k
+    # each compute_done comes after the previous one
+    for i in range(1, 4):
+        assert done[i - 1].elapsed_time(done[i]) > 0.0
