@@ -77,6 +77,15 @@ typedef enum { LCE_REDUCTION_MEAN = 0, LCE_REDUCTION_SUM = 1 } lce_reduction_t;
 typedef enum { LCE_BF16 = 0, LCE_F32 = 1, LCE_F32_TF32X3 = 2 } lce_dtype_t;
 
 /*
+ * Width of the vocabulary strips (columns): the vocabulary is cut into ceil(V / strip_V) strips
+ * of equal width -- every strip but the last is this wide, the last one the rest -- rounded up to
+ * the tensor cores' tile width of 256 columns (128 for LCE_F32) when that stays within strip_V,
+ * else to 128; never wider than strip_V or V.  strip_V is thus the largest strip, and the last
+ * strip is never a sliver.  0 when V < 1 or strip_V breaks its shape rule.
+ */
+int64_t lce_strip_columns(int64_t V, int64_t strip_V, lce_dtype_t dtype);
+
+/*
  * Bytes of device workspace that lce_forward and lce_backward need for these sizes; 0 when the
  * arguments break a shape rule.  It grows as O(N * min(strip_V, V)) (LCE_F32_TF32X3 adds
  * O((N + min(strip_V, V)) * d) for its operand copies) and never with V beyond the strip: this
@@ -96,9 +105,9 @@ typedef enum { LCE_BF16 = 0, LCE_F32 = 1, LCE_F32_TF32X3 = 2 } lce_dtype_t;
 size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dtype);
 
 /*
- * Forward.  Visits the vocabulary in strips of strip_V columns; for each strip it forms the
- * logit tiles (tensor cores; CUDA cores for LCE_F32), folds them into the running per-token
- * state in the GEMM epilogue and drops them.  Writes
+ * Forward.  Visits the vocabulary in strips of lce_strip_columns(V, strip_V, dtype) columns; for
+ * each strip it forms the logit tiles (tensor cores; CUDA cores for LCE_F32), folds them into the
+ * running per-token state in the GEMM epilogue and drops them.  Writes
  *   loss    : device fp32 scalar (MEAN over valid rows; NaN when n_valid == 0.  SUM: the sum)
  *   lse     : device fp32 [N], log-sum-exp of every row (ignored rows included)
  *   n_valid : device int64 scalar, number of rows whose label is in [0, V)

@@ -18,7 +18,7 @@ def full_logits_bytes(tokens: int, vocab: int, bytes_per_element: int = 4) -> in
 def __getattr__(name):
     # The binding is imported lazily so that host-only users (input recipes, sizes) do not need
     # torch.cuda; it never falls back to anything when the library is missing.
-    if name in ("lce_workspace_size", "lce_forward", "lce_backward", "lce_check_error",
+    if name in ("lce_workspace_size", "lce_strip_columns", "lce_forward", "lce_backward", "lce_check_error",
                 "lce_host_buffer_size", "lce_forward_backward_host", "lce_launch_count",
                 "linear_cross_entropy", "LinearCrossEntropy"):
         from . import api

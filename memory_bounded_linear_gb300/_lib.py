@@ -26,6 +26,7 @@ _c_i64 = ctypes.c_int64
 _c_p = ctypes.c_void_p
 _SIGNATURES = {
     "lce_workspace_size": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int]),
+    "lce_strip_columns": (ctypes.c_int64, [_c_i64, _c_i64, ctypes.c_int]),
     "lce_forward": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64,
                                    ctypes.c_int, ctypes.c_int, _c_p, _c_p, _c_p, _c_p,
                                    ctypes.c_size_t, _c_p]),

@@ -69,6 +69,11 @@ def lce_workspace_size(N: int, d: int, V: int, strip_V: int, dtype: str = "bf16"
     return int(_lib.load().lce_workspace_size(N, d, V, strip_V, _lib.DTYPES[dtype]))
 
 
+def lce_strip_columns(V: int, strip_V: int, dtype: str = "bf16") -> int:
+    """Width of the vocabulary strips for these sizes (0 on a bad argument)."""
+    return int(_lib.load().lce_strip_columns(V, strip_V, _lib.DTYPES[dtype]))
+
+
 def lce_forward(H, W, labels, *, ignore_index: int = -100, strip_V: int = 8192,
                 reduction: str = "mean", workspace: Optional[torch.Tensor] = None,
                 stream: Optional[torch.cuda.Stream] = None, out=None, f32_mode: str = "exact"):

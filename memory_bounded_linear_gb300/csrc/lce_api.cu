@@ -25,7 +25,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
   int bn;           // logit tile width of the engine
-  int64_t w;        // effective strip width min(strip_V, V)
+  int64_t w;        // strip width (strip_columns): every strip but the last is w columns wide
   int64_t ldg;      // row stride of the strip gradient workspace (elements)
   int tiles;        // logit tiles per full strip
   size_t off_run, off_tgt, off_part, off_g;
@@ -52,13 +52,26 @@ bool shape_ok(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dt) 
   return true;
 }
 
+// Width of the strips: the vocabulary is cut into ceil(V / strip_V) strips of equal width, rounded
+// up to the tile width of the engine (so that only the last strip ends inside a tile) when that
+// stays within strip_V, else to 128 columns; never wider than strip_V or V.  With strips of
+// strip_V columns the last one could be a sliver (4,096 of 151,552 columns at strip 16,384) whose
+// launches fill the GPU poorly.
+int64_t strip_columns(int64_t V, int64_t strip_V, int bn) {
+  const int64_t S = (V + strip_V - 1) / strip_V;
+  const int64_t even = (V + S - 1) / S;
+  int64_t w = (even + bn - 1) / bn * bn;
+  if (w > strip_V) w = (even + 127) / 128 * 128;
+  return std::min(w, V);
+}
+
 bool make_layout(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dt, Layout* L) {
   if (dt != LCE_BF16 && dt != LCE_F32 && dt != LCE_F32_TF32X3) return false;
   if (!shape_ok(N, d, V, strip_V, dt)) return false;
   const bool x3 = (dt == LCE_F32_TF32X3);
   *L = Layout{};
   L->bn = (dt == LCE_F32) ? SIMT_BN : TC_BN;
-  L->w = std::min(strip_V, V);
+  L->w = strip_columns(V, strip_V, L->bn);
   L->ldg = (L->w + L->bn - 1) / L->bn * L->bn;
   L->tiles = static_cast<int>((L->w + L->bn - 1) / L->bn);
   L->ldt = (N + 31) / 32 * 32;
@@ -286,6 +299,12 @@ using namespace lce;
 
 extern "C" {
 
+int64_t lce_strip_columns(int64_t V, int64_t strip_V, lce_dtype_t dtype) {
+  if (dtype != LCE_BF16 && dtype != LCE_F32 && dtype != LCE_F32_TF32X3) return 0;
+  if (V < 1 || V > kMaxDim || strip_V < 128 || strip_V % 128 != 0 || strip_V > kMaxDim) return 0;
+  return strip_columns(V, strip_V, dtype == LCE_F32 ? SIMT_BN : TC_BN);
+}
+
 size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, int64_t strip_V, lce_dtype_t dtype) {
   Layout L;
   if (!make_layout(N, d, V, strip_V, dtype, &L)) return 0;
@@ -314,8 +333,8 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels, in
   if (note(cudaMemsetAsync(ws, 0, WS_HEADER_BYTES, stream)) != cudaSuccess) return LCE_ERR_CUDA;
 
   // The forward keeps one (max, sum-exp) partial per token and logit tile of the columns a launch
-  // covers.  When the partials of the whole vocabulary fit in the workspace sized for strip_V (the
-  // backward's gradient strip is larger whenever strip_V >= V/64), one persistent launch covers
+  // covers.  When the partials of the whole vocabulary fit in the workspace sized for the strip
+  // width (the backward's gradient strip is larger whenever it is >= V/64), one persistent launch covers
   // every strip; otherwise there is one launch per strip.  Either way the workspace is the same.
   // LCE_F32_TF32X3 splits W one strip at a time, so it keeps one launch per strip.
   const bool x3 = (dtype == LCE_F32_TF32X3);
@@ -323,7 +342,7 @@ lce_status_t lce_forward(const void* H, const void* W, const int64_t* labels, in
   const bool one_launch =
       !x3 && L.off_part + static_cast<size_t>(tiles_all) * static_cast<size_t>(N) * sizeof(float2) <=
                  L.total;
-  const int64_t fwd_step = one_launch ? V : strip_V;
+  const int64_t fwd_step = one_launch ? V : L.w;
   if (N > 0) {
     if (x3 && split(H, static_cast<size_t>(N) * d, ws, L.off_h, L.h_part, stream) != cudaSuccess)
       return LCE_ERR_CUDA;
@@ -404,10 +423,10 @@ lce_status_t backward_impl(const void* H, const void* W, const int64_t* labels, 
   }
   auto strip_job = [&](int64_t s, int mode, void* g) {
     StripArgs a{};
-    const int64_t col0 = s * strip_V;
+    const int64_t col0 = s * L.w;
     a.mode = mode;
     a.col0 = static_cast<int>(col0);
-    a.strip_cols = static_cast<int>(std::min(strip_V, V - col0));
+    a.strip_cols = static_cast<int>(std::min(L.w, V - col0));
     a.H = H; a.W = W; a.d = d; a.N = N; a.V = V;
     a.G = g; a.ldg = L.ldg;
     a.labels = labels; a.ignore_index = ignore_index;
@@ -421,7 +440,7 @@ lce_status_t backward_impl(const void* H, const void* W, const int64_t* labels, 
     }
     return a;
   };
-  const int64_t S = (V + strip_V - 1) / strip_V;
+  const int64_t S = (V + L.w - 1) / L.w;
   auto run = [&](StripArgs* jobs, int nj) {
     bool grad = false, dhdw = false;
     for (int j = 0; j < nj; ++j) (jobs[j].mode == MODE_BWD_G ? grad : dhdw) = true;
@@ -443,7 +462,7 @@ lce_status_t backward_impl(const void* H, const void* W, const int64_t* labels, 
       if (want_dh) jobs[nj++] = strip_job(s, MODE_DH, nullptr);
       if (want_dw) jobs[nj++] = strip_job(s, MODE_DW, nullptr);
       for (int j = 0; j < nj; ++j) set_x3_operands(jobs[j], ws, L);
-      const float* w_strip = static_cast<const float*>(W) + static_cast<size_t>(s * strip_V) * d;
+      const float* w_strip = static_cast<const float*>(W) + static_cast<size_t>(s * L.w) * d;
       if (split(w_strip, static_cast<size_t>(grad.strip_cols) * d, ws, L.off_w, L.w_part,
                 stream) != cudaSuccess ||
           (want_dh && split_t(w_strip, grad.strip_cols, d, L.ldg, ws, L.off_wt, L.wt_part,
@@ -482,7 +501,7 @@ lce_status_t backward_impl(const void* H, const void* W, const int64_t* labels, 
     }
     return LCE_OK;
   }
-  for (int64_t col0 = 0, s = 0; col0 < V; col0 += strip_V, ++s) {
+  for (int64_t col0 = 0, s = 0; col0 < V; col0 += L.w, ++s) {
     StripArgs a = strip_job(s, MODE_BWD_G, G);
     a.mode = MODE_BWD_G;
     if (strip_gemm(a, dtype, stream, num_sms) != cudaSuccess) return LCE_ERR_CUDA;

@@ -44,11 +44,38 @@ def _ws(lib, N, d, V, s, dt=0):
     return lib.lce_workspace_size(N, d, V, s, dt)
 
 
+def _strip(V, s, bn):
+    """The strip width the header states: ceil(V / s) strips of equal width, rounded up to the
+    engine's tile width bn when that stays within s, else to 128; at most V."""
+    S = -(-V // s)
+    even = -(-V // S)
+    w = -(-even // bn) * bn
+    if w > s:
+        w = -(-even // 128) * 128
+    return min(w, V)
+
+
+@pytest.mark.parametrize("V,s,bn,want", [(151552, 16384, 256, 15360), (151936, 8192, 256, 8192),
+                                         (151936, 4096, 256, 4096), (151936, 32768, 256, 30464),
+                                         (200000, 16384, 256, 15616), (1000, 384, 256, 384),
+                                         (300, 4096, 256, 300), (40000, 128, 256, 128),
+                                         (4096, 512, 128, 512), (131072, 16384, 256, 16384)])
+def test_strip_columns(lib, V, s, bn, want):
+    """Equal strips: the last strip is never a sliver, no strip is wider than strip_V."""
+    assert _strip(V, s, bn) == want
+    dt = 0 if bn == 256 else 1
+    assert lib.lce_strip_columns(V, s, dt) == want
+    S = -(-V // want)
+    assert want <= s and S == -(-V // s)          # as many strips as strip_V gives
+    assert V - (S - 1) * want > 0                  # the last strip is not empty
+    assert lib.lce_strip_columns(V, 100, 0) == 0 and lib.lce_strip_columns(0, 128, 0) == 0
+
+
 def test_workspace_size_formula(lib):
     # bf16, large backward step (128 x 24 dH tiles > 512): header + max(forward state, one strip
     # of bf16 gradient rows padded to 256 columns)
     N, d, V, s = 32768, 6144, 151552, 16384
-    g_bytes = N * 16384 * 2
+    g_bytes = N * 15360 * 2   # ten strips of 15360 columns (the last one 13312)
     assert _ws(lib, N, d, V, s) == 256 + g_bytes
     # bf16, small backward step (16 x 8 dH tiles): two gradient strips, consecutive strips overlap
     assert _ws(lib, 4096, 2048, 151936, 8192) == 256 + 2 * 4096 * 8192 * 2
@@ -66,7 +93,7 @@ def test_workspace_size_tf32x3(lib):
     # of the gradient strip and of the gradient strip transposed)
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     for N, d, V, s in [(16384, 7168, 200000, 16384), (100, 64, 300, 4096), (33, 8, 1000, 128)]:
-        w = min(s, V)
+        w = _strip(V, s, 256)
         ldg = (w + 255) // 256 * 256
         ldt = (N + 31) // 32 * 32
         split = 2 * r(N * d * 4) + 2 * r(w * d * 4)

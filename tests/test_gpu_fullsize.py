@@ -7,7 +7,7 @@ C-ABI calls as bench.py), against the float64 oracle on every configuration:
 * n_valid exactly, and the loss against the oracle's loss (its lse and target logits);
 * dH on seeded samples of token rows (each row needs only its own logits);
 * dW on samples of vocabulary rows: the most frequent labels, outlier rows of W (rows whose norm
-  stands out), the rows on both sides of every strip boundary, the last row, and seeded random
+  stands out), the rows on both sides of every strip boundary (lce_strip_columns), the last row, and seeded random
   rows -- a dW tile written to the wrong place, or a wrong long reduction over the tokens, shows
   there;
 * and, on the full gradients, properties that hold at any size: sum_v dW_v = 0 and
@@ -91,7 +91,8 @@ def _check(w, strip_V, n_rows=48, n_vocab=24, f32_mode="exact"):
     norms = np.linalg.norm(Wn, axis=1)
     outliers = np.nonzero(norms > 4.0 * np.median(norms))[0]
     assert (outliers.size > 0) == (w.outlier_frac > 0)
-    bounds = np.arange(strip_V, w.V, strip_V)
+    width = api.lce_strip_columns(w.V, strip_V, "tf32x3" if f32_mode == "tf32x3" else w.dtype)
+    bounds = np.arange(width, w.V, width)
     vs = np.concatenate([np.argsort(-counts)[:8], outliers[:8], bounds - 1, bounds, [w.V - 1],
                          rng.choice(w.V, n_vocab, replace=False)])
     vs = np.unique(vs[(vs >= 0) & (vs < w.V)])
@@ -129,7 +130,9 @@ def test_n65536_d2048_v151936_strip_sweep(cuda_lib, strip):
     extra = _check(w, strip, n_rows=32, n_vocab=16)
     outputs = w.N * 4 + w.N * w.d * 4 + w.V * w.d * 4       # lse, dH, dW
     ws = api.lce_workspace_size(w.N, w.d, w.V, strip)
-    assert ws >= w.N * strip * 2                            # one bf16 gradient strip
+    width = api.lce_strip_columns(w.V, strip)
+    assert strip - 256 < width <= strip                     # equal strips, none wider than strip
+    assert ws >= w.N * width * 2                            # one bf16 gradient strip
     assert extra <= outputs + ws + 4 * 1024 * 1024
     assert extra - outputs < w.N * w.V * 4 / 4              # far below the N x V fp32 logits
 
