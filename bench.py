@@ -73,20 +73,14 @@ KERNEL_SOURCES = ("memory_bounded_linear_gb300/csrc/lce_tc.cu",
                   "memory_bounded_linear_gb300/csrc/ptx.cuh",
                   "memory_bounded_linear_gb300/csrc/lce_internal.h",
                   "memory_bounded_linear_gb300/csrc/lce_api.cu")  # launch structure
-KERNEL_SOURCE_SHA256 = "b9fb46b17d5d5bef176c3fe01bd9aa1e6fa69cd06ce35c28a222a0aae7e71acf"
+KERNEL_SOURCE_SHA256 = "97ff1688a1f5e666fb9e0806d74e3b692fd2c12ec2981123abdfef72ac1af6d9"
 MEASURED_TRAFFIC = {
-    # N=32768 d=6144 V=151552, strip 16384: the timed step's 21 launches -- the forward over the
-    # whole vocabulary, then per strip the gradient launch and the dW + dH launch (each averaged
-    # over its 10 launches, the 4096-column tail strip included)
-    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse", "bf16"): 30413000000,
-    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd_grad", "bf16"): 4475000000,
-    ("n32768-d6144-v151552-outliers", 16384, "tc_dh_dw", "bf16"): 18763000000,
-    # N=16384 d=7168 V=200000 fp32, three-product tf32, strip 16384: the timed step's 39
-    # tensor-core launches -- 13 forward strips, then per strip the gradient launch and the
-    # dH + dW launch (each averaged over its 13 launches)
-    ("n16384-d7168-v200000-fp32", 16384, "tc_fwd_lse", "tf32x3"): 17367000000,
-    ("n16384-d7168-v200000-fp32", 16384, "tc_bwd_grad", "tf32x3"): 20908000000,
-    ("n16384-d7168-v200000-fp32", 16384, "tc_dh_dw", "tf32x3"): 54171000000,
+    # N=32768 d=6144 V=151552, strip 16384 (ten strips of 15360 columns, the last 13312): the
+    # timed step's 21 launches -- the forward over the whole vocabulary, then per strip the
+    # gradient launch and the dW + dH launch (each averaged over its 10 launches)
+    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse", "bf16"): 30451000000,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd_grad", "bf16"): 4493000000,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_dh_dw", "bf16"): 17701000000,
 }
 
 
@@ -437,8 +431,10 @@ def main():
     #  * e2e_loss_only (the training-loop figure): the same calls, but only the loss and the error
     #    flags come back; dH and dW stay on the device, where the previous layer's backward and the
     #    optimizer would use them.
-    # Consecutive steps alternate between two device buffers and two streams, so the copies of one
-    # step overlap the kernels of the other.
+    # Consecutive steps rotate over three device buffers and three streams, and each step's kernels
+    # wait for the previous step's (compute_after / compute_done): the kernels run one step at a
+    # time while the copies in of one step and the copies out of another proceed beside them on
+    # the two copy directions.
     e2e = e2e_loss = None
     if not args.no_e2e:
         Hh = H.cpu().pin_memory()
@@ -447,31 +443,31 @@ def main():
         dl = torch.ones((), dtype=torch.float32).pin_memory()
         in_bytes = sum(t.numel() * t.element_size() for t in (Hh, Wh, yh, dl))
         hb = api.lce_host_buffer_size(N, d, V, S, dt)
-        dbufs = [torch.empty(hb, dtype=torch.uint8, device=dev) for _ in range(2)]
-        streams = [torch.cuda.Stream(dev) for _ in range(2)]
+        NB = 3
+        dbufs = [torch.empty(hb, dtype=torch.uint8, device=dev) for _ in range(NB)]
+        streams = [torch.cuda.Stream(dev) for _ in range(NB)]
         houts = [{"loss": torch.empty((), dtype=torch.float32).pin_memory(),
                   "lse": torch.empty(N, dtype=torch.float32).pin_memory(),
                   "n_valid": torch.empty((), dtype=torch.int64).pin_memory(),
                   "dH": torch.empty(N, d, dtype=torch.float32).pin_memory(),
                   "dW": torch.empty(V, d, dtype=torch.float32).pin_memory(),
-                  "flags": torch.zeros(1, dtype=torch.int32).pin_memory()} for _ in range(2)]
+                  "flags": torch.zeros(1, dtype=torch.int32).pin_memory()} for _ in range(NB)]
 
-        done = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(NB)]
 
         def run_steps(k, results_back):
             for i in range(k):
-                o = houts[i % 2]
+                o = houts[i % NB]
                 outs = o if results_back else {"loss": o["loss"], "flags": o["flags"]}
-                # this step's kernels start after the previous step's have finished: the copies
-                # overlap the other step's kernels, the kernels run one step at a time
-                api.lce_forward_backward_host(Hh, Wh, yh, dl, device_buffer=dbufs[i % 2],
+                # this step's kernels start after the previous step's have finished
+                api.lce_forward_backward_host(Hh, Wh, yh, dl, device_buffer=dbufs[i % NB],
                                               strip_V=S, reduction=w.reduction, f32_mode=fm,
-                                              stream=streams[i % 2],
-                                              compute_after=done[(i + 1) % 2] if i else None,
-                                              compute_done=done[i % 2], **outs)
+                                              stream=streams[i % NB],
+                                              compute_after=done[(i - 1) % NB] if i else None,
+                                              compute_done=done[i % NB], **outs)
 
         def time_e2e(results_back):
-            run_steps(2, results_back)
+            run_steps(NB, results_back)
             barrier()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -495,16 +491,16 @@ def main():
                "ms_per_step": e_ms, "api": "lce_forward_backward_host",
                "results": "loss, lse, n_valid, dH, dW and error flags copied back to pinned host "
                           "memory every step",
-               "overlap": "two device buffers and two streams alternating by step; each step's "
-                          "kernels wait for the previous step's (compute_after / compute_done)"}
+               "overlap": "three device buffers and streams rotating by step; each step's kernels "
+                          "wait for the previous step's (compute_after / compute_done)"}
         l_ms = time_e2e(False)
         e2e_loss = {"value": tokens_per_second(world, N, l_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4 + 4,
                     "ms_per_step": l_ms, "api": "lce_forward_backward_host",
                     "results": "loss and error flags only; dH and dW stay on the device "
                                "(training-loop figure)",
-                    "overlap": "two device buffers and two streams alternating by step; each "
-                               "step's kernels wait for the previous step's"}
+                    "overlap": "three device buffers and streams rotating by step; each step's "
+                               "kernels wait for the previous step's"}
         del dbufs, houts
 
     # Delayed weight gradient (lce_backward_parts): the dgrad-only and wgrad-only backward calls
