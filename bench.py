@@ -81,6 +81,12 @@ MEASURED_TRAFFIC = {
     ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse", "bf16"): 30451000000,
     ("n32768-d6144-v151552-outliers", 16384, "tc_bwd_grad", "bf16"): 4493000000,
     ("n32768-d6144-v151552-outliers", 16384, "tc_dh_dw", "bf16"): 17701000000,
+    # N=16384 d=7168 V=200000 fp32, three-product tf32, strip 16384 (13 strips of 15616 columns,
+    # the last 12608): the timed step's 39 tensor-core launches -- 13 forward strips, then per
+    # strip the gradient launch and the dH + dW launch (each averaged over its 13 launches)
+    ("n16384-d7168-v200000-fp32", 16384, "tc_fwd_lse", "tf32x3"): 14452000000,
+    ("n16384-d7168-v200000-fp32", 16384, "tc_bwd_grad", "tf32x3"): 19917000000,
+    ("n16384-d7168-v200000-fp32", 16384, "tc_dh_dw", "tf32x3"): 48165000000,
 }
 
 
