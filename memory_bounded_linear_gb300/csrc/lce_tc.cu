@@ -234,6 +234,11 @@ struct TileQueue {
   unsigned* err;
   int slot;
   uint32_t ph;
+  // a reader in the second CTA of a pair: it hands slots back to the first CTA's barrier with a
+  // cluster-scope release; readers in the first CTA hand back locally with a CTA-scope release,
+  // which does not make them wait the way the cluster-scope one does (measured: the MMA thread
+  // spent 5-14% of its time in a cluster-scope hand-back)
+  bool remote;
 
   __device__ __forceinline__ void advance() {
     if (++slot == TQ) { slot = 0; ph ^= 1u; }
@@ -270,7 +275,7 @@ struct TileQueue {
     __syncwarp(mask);
     if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(mask) - 1)) {
       const uint32_t empty = ptx::smem_addr(&ctl->tq_empty[slot]);
-      if (PAIR) ptx::mbar_arrive_cluster(ptx::mapa_shared(empty, 0));
+      if (remote) ptx::mbar_arrive_cluster(ptx::mapa_shared(empty, 0));
       else ptx::mbar_arrive(empty);
     }
     advance();
@@ -509,13 +514,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       bool ok = true;
       Ring ring{0, 0u};
-      TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u};
-      unsigned next = (rank == 0) ? atomicAdd(&p.sched[0], 1u) : 0u;
+      TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u, PAIR && rank != 0};
+      // The first CTA posts every tile's ticket one tile ahead: when it starts loading tile t, the
+      // ticket of tile t+1 is already in the ring, so the readers (and the peer CTA's producer)
+      // find it there at the tile boundary; the counter is read one more tile ahead still.
+      unsigned next = 0u;
+      int upcoming = -1;
+      if (rank == 0) {
+        next = atomicAdd(&p.sched[0], 1u);
+        upcoming = tq.post(next, p.sched, p.total_tiles, units);
+        if (upcoming >= 0) next = atomicAdd(&p.sched[0], 1u);
+      }
       while (ok) {
         int tile;
         if (rank == 0) {
-          tile = tq.post(next, p.sched, p.total_tiles, units);
-          if (tile >= 0) next = atomicAdd(&p.sched[0], 1u);  // used once this tile is loaded
+          tile = upcoming;
+          if (tile < 0) break;
+          upcoming = tq.post(next, p.sched, p.total_tiles, units);
+          if (upcoming >= 0) next = atomicAdd(&p.sched[0], 1u);
         } else {
           tile = tq.take(1u);
         }
@@ -543,7 +559,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       Ring ring{0, 0u};
       int acc = 0;
       uint32_t aph = 0;
-      TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u};
+      TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u, PAIR && rank != 0};
       while (ok) {
         const int tile = tq.take(1u);
         if (tile < 0) break;
@@ -585,7 +601,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     int acc = 0;
     uint32_t aph = 0;
-    TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u};
+    TileQueue<PAIR> tq{ctl, abort_flag, p.err, 0, 0u, PAIR && rank != 0};
     while (true) {
       const int tile = tq.take(0xffffffffu);
       if (tile < 0) break;
