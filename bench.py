@@ -73,20 +73,20 @@ KERNEL_SOURCES = ("memory_bounded_linear_gb300/csrc/lce_tc.cu",
                   "memory_bounded_linear_gb300/csrc/ptx.cuh",
                   "memory_bounded_linear_gb300/csrc/lce_internal.h",
                   "memory_bounded_linear_gb300/csrc/lce_api.cu")  # launch structure
-KERNEL_SOURCE_SHA256 = "97ff1688a1f5e666fb9e0806d74e3b692fd2c12ec2981123abdfef72ac1af6d9"
+KERNEL_SOURCE_SHA256 = "649966d7e5fcd986904d7a1bde41bc8be0ff22df4e4985d2f313c6bd396c7890"
 MEASURED_TRAFFIC = {
     # N=32768 d=6144 V=151552, strip 16384 (ten strips of 15360 columns, the last 13312): the
     # timed step's 21 launches -- the forward over the whole vocabulary, then per strip the
     # gradient launch and the dW + dH launch (each averaged over its 10 launches)
-    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse", "bf16"): 30451000000,
-    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd_grad", "bf16"): 4493000000,
-    ("n32768-d6144-v151552-outliers", 16384, "tc_dh_dw", "bf16"): 17701000000,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_fwd_lse", "bf16"): 30406000000,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_bwd_grad", "bf16"): 4437000000,
+    ("n32768-d6144-v151552-outliers", 16384, "tc_dh_dw", "bf16"): 20225000000,
     # N=16384 d=7168 V=200000 fp32, three-product tf32, strip 16384 (13 strips of 15616 columns,
     # the last 12608): the timed step's 39 tensor-core launches -- 13 forward strips, then per
     # strip the gradient launch and the dH + dW launch (each averaged over its 13 launches)
-    ("n16384-d7168-v200000-fp32", 16384, "tc_fwd_lse", "tf32x3"): 14452000000,
-    ("n16384-d7168-v200000-fp32", 16384, "tc_bwd_grad", "tf32x3"): 19917000000,
-    ("n16384-d7168-v200000-fp32", 16384, "tc_dh_dw", "tf32x3"): 48165000000,
+    ("n16384-d7168-v200000-fp32", 16384, "tc_fwd_lse", "tf32x3"): 14557000000,
+    ("n16384-d7168-v200000-fp32", 16384, "tc_bwd_grad", "tf32x3"): 18253000000,
+    ("n16384-d7168-v200000-fp32", 16384, "tc_dh_dw", "tf32x3"): 46299000000,
 }
 
 
