@@ -491,6 +491,33 @@ def main():
             return max_over_ranks(e0.elapsed_time(e1) / k2, world, dev)
 
         out_bytes = sum(t.numel() * t.element_size() for t in houts[0].values())
+
+        def copy_gbs():
+            """The box's pinned-memory copy rate, copies alone (no kernels), with the same pinned
+            buffers: dH and dW back (device to host), H and W in (host to device)."""
+            st = streams[0]
+            as_bytes = [t.reshape(-1).view(torch.uint8)
+                        for t in (houts[0]["dH"], houts[0]["dW"], Hh, Wh)]
+            pairs_d2h = [(o, dbufs[0][:o.numel()]) for o in as_bytes[:2]]
+            pairs_h2d = [(dbufs[0][:t.numel()], t) for t in as_bytes[2:]]
+            rates = {}
+            for name, pairs in (("d2h", pairs_d2h), ("h2d", pairs_h2d)):
+                nbytes = sum(dst.numel() for dst, _ in pairs)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(st):
+                    for dst, src in pairs:
+                        dst.copy_(src, non_blocking=True)
+                    e0.record(st)
+                    for _ in range(3):
+                        for dst, src in pairs:
+                            dst.copy_(src, non_blocking=True)
+                    e1.record(st)
+                st.synchronize()
+                rates[name] = 3 * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
+            return rates
+
+        copy_rates = copy_gbs()
         e_ms = time_e2e(True)
         e2e = {"value": tokens_per_second(world, N, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
@@ -498,7 +525,8 @@ def main():
                "results": "loss, lse, n_valid, dH, dW and error flags copied back to pinned host "
                           "memory every step",
                "overlap": "three device buffers and streams rotating by step; each step's kernels "
-                          "wait for the previous step's (compute_after / compute_done)"}
+                          "wait for the previous step's (compute_after / compute_done)",
+               "copy_gbs_alone": copy_rates}
         l_ms = time_e2e(False)
         e2e_loss = {"value": tokens_per_second(world, N, l_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4 + 4,
