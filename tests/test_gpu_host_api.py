@@ -153,3 +153,34 @@ def test_host_calls_chained_by_compute_events(cuda_lib):
     # each compute_done comes after the previous one
     for i in range(1, 4):
         assert done[i - 1].elapsed_time(done[i]) > 0.0
+
+
+def _same(a, b):
+    """Bitwise equality that treats NaN as equal to NaN (the mean loss of an empty batch)."""
+    if a.shape != b.shape or not torch.equal(torch.isnan(a), torch.isnan(b)):
+        return False
+    return torch.equal(torch.nan_to_num(a, nan=0.0), torch.nan_to_num(b, nan=0.0))
+
+
+@pytest.mark.parametrize("fmt,mode", [("bf16", "exact"), ("f32", "exact"), ("f32", "tf32x3")],
+                         ids=["bf16", "f32", "tf32x3"])
+def test_host_entry_point_degenerate_shapes(cuda_lib, fmt, mode):
+    """An empty batch, one token, and a one-word vocabulary through the host entry point: every
+    result bitwise that of the device entry points on the same inputs, no error flag, and the
+    closed forms of those cases (no valid row: n_valid 0 and dW 0; V = 1: loss and gradients
+    0 within rounding)."""
+    base = W2 if fmt == "bf16" else WT
+    for N, d, V in [(0, 64, 300), (1, 16, 2), (130, 24, 1)]:
+        w = base.with_sizes(N=N, d=d, V=V, strip_V=128)
+        H, W, y = make_inputs(w, "cpu", seed=3)
+        out = _host_run(H, W, y, w, mode)
+        torch.cuda.synchronize()
+        ref = _device_run(H, W, y, w, mode)
+        assert int(out["flags"].item()) == 0, (N, d, V)
+        for k in ("loss", "lse", "n_valid", "dH", "dW"):
+            assert _same(out[k], ref[k]), (N, d, V, k)
+        if N == 0:
+            assert int(out["n_valid"].item()) == 0 and torch.count_nonzero(out["dW"]).item() == 0
+        if V == 1:  # zero up to the rounding of the base-2 log-sum-exp
+            assert abs(out["loss"].item()) < 1e-6
+            assert out["dH"].abs().max().item() < 1e-6 and out["dW"].abs().max().item() < 1e-6
