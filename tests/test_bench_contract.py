@@ -1,7 +1,7 @@
 """bench.py's host side, on the CPU: the JSON line of the reference arm (the float64 oracle timed
-on host cores) carries every key of the benchmark contract and at least 3 warm-up steps, and the per-kernel FLOP factors that
-the roofline figures use add up to the 8 N d V of a forward + backward for every launch
-structure the library uses."""
+on host cores) carries every key of the benchmark contract and at least 3 warm-up steps, and the
+per-kernel FLOP factors that the roofline figures use add up to the 8 N d V of a forward +
+backward for every launch structure the library uses."""
 
 import json
 import os
